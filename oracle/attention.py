@@ -1,0 +1,167 @@
+"""Plain fp64 attention: forward, standard backward, D, and the two-half merge.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the CUDA library never
+imports this module, and this module imports nothing from the library.
+
+Layout: every 4-D array is [B, H, S, d] (float64), L and D are [B, H, S].
+Self-attention only: N_q = N_k = S.  Inputs are widened exactly to float64 by
+the caller from the values the GPU sees (bf16- or fp32-rounded).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "scores", "causal_keep", "attention_fwd", "attention_fwd_rows", "attention_bwd",
+    "rowsum_o_do", "partial_attention", "merge_two_halves",
+]
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def causal_keep(n_q: int, n_k: int) -> np.ndarray:
+    """Boolean [n_q, n_k]: True where key j may be attended by query i (j <= i).
+
+    "CS336 Assignment 2: Systems" (blog), FlashAttention-2 Triton kernel: an
+    entry is masked when the query index is smaller than the key index.  The
+    handout's ``flash_forward`` (c) adds -1e6 to masked scores; here masked
+    entries are excluded outright (-inf), which gives the same softmax because
+    the diagonal is always kept.
+    """
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_k)[None, :]
+    return j <= i
+
+
+def scores(q_bh: np.ndarray, k_bh: np.ndarray, scale: float) -> np.ndarray:
+    """S = Q K^T * scale for one (batch, head): handout Eq. 4 (scale = 1/sqrt(d) there)."""
+    return (_f64(q_bh) @ _f64(k_bh).T) * float(scale)
+
+
+def _softmax_and_lse(S: np.ndarray, keep):
+    """Row softmax P (handout Eq. 5) and logsumexp L (Eq. 12) of one score matrix.
+
+    L_i = log sum_j exp(S_ij) over the kept j, evaluated in the stable form
+    m_i + log sum_j exp(S_ij - m_i) with m_i the row maximum.
+    """
+    if keep is not None:
+        S = np.where(keep, S, -np.inf)
+    m = S.max(axis=1, keepdims=True)
+    e = np.exp(S - m)                      # excluded entries give exp(-inf) = 0
+    l = e.sum(axis=1, keepdims=True)
+    P = e / l
+    L = m[:, 0] + np.log(l[:, 0])
+    return P, L
+
+
+def attention_fwd(q, k, v, causal: bool, scale: float):
+    """O = softmax(Q K^T * scale) V and L = logsumexp of the scaled scores.
+
+    Handout Eq. 4-6 and Eq. 12, one (b, h) slice at a time, full S x S matrix.
+    Returns (O [B,H,S,d], L [B,H,S]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, S, d = q.shape
+    keep = causal_keep(S, S) if causal else None
+    O = np.empty_like(q)
+    L = np.empty((B, H, S))
+    for b in range(B):
+        for h in range(H):
+            P, Lbh = _softmax_and_lse(scores(q[b, h], k[b, h], scale), keep)
+            O[b, h] = P @ v[b, h]
+            L[b, h] = Lbh
+    return O, L
+
+
+def attention_fwd_rows(q_bh, k_bh, v_bh, rows, causal: bool, scale: float):
+    """The same definition for a chosen set of query rows of one (b, h) slice.
+
+    Each output row depends only on its own query row and on all of K, V
+    (handout Eq. 4-6), so sampled rows of a large problem are computed exactly
+    without forming the whole score matrix.  Returns (O_rows [r,d], L_rows [r]).
+    """
+    q_bh, k_bh, v_bh = _f64(q_bh), _f64(k_bh), _f64(v_bh)
+    rows = np.asarray(rows, dtype=np.int64)
+    S = scores(q_bh[rows], k_bh, scale)                  # [r, S]
+    keep = (np.arange(k_bh.shape[0])[None, :] <= rows[:, None]) if causal else None
+    P, L = _softmax_and_lse(S, keep)
+    return P @ v_bh, L
+
+
+def attention_bwd(q, k, v, do, causal: bool, scale: float):
+    """dQ, dK, dV by the standard backward pass, handout Eq. 7-11.
+
+    P is recomputed by the plain forward definition, then
+      dV = P^T dO                              (Eq. 7)
+      dP = dO V^T                              (Eq. 8)
+      dS_i = (diag(P_i) - P_i P_i^T) dP_i      (Eq. 9), i.e. P_i*dP_i - P_i (P_i . dP_i)
+      dQ = dS K * scale                        (Eq. 10)
+      dK = dS^T Q * scale                      (Eq. 11)
+    The D shortcut of Eq. 13-19 is deliberately not used here; the pins check
+    separately that P_i . dP_i equals D_i = rowsum(O * dO)_i.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, S, d = q.shape
+    keep = causal_keep(S, S) if causal else None
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    for b in range(B):
+        for h in range(H):
+            P, _ = _softmax_and_lse(scores(q[b, h], k[b, h], scale), keep)
+            dv[b, h] = P.T @ do[b, h]
+            dP = do[b, h] @ v[b, h].T
+            dS = P * dP - P * np.sum(P * dP, axis=1, keepdims=True)
+            dq[b, h] = (dS @ k[b, h]) * scale
+            dk[b, h] = (dS.T @ q[b, h]) * scale
+    return dq, dk, dv
+
+
+def rowsum_o_do(o, do) -> np.ndarray:
+    """D = rowsum(O * dO), handout section 4 "Backward pass with recomputation"
+    (computed once before the backward loops, Algorithm 2 step 2)."""
+    return np.sum(_f64(o) * _f64(do), axis=-1)
+
+
+def partial_attention(q_bh, k_bh, v_bh, key_idx, causal: bool, scale: float):
+    """Softmax pieces of one key subset, in the notation of the two-half merge.
+
+    "[Attention] FlashAttention/Ring-Attention/...统一原理": for the keys in
+    ``key_idx`` take x = the scaled scores, m = their row maximum, the
+    numerators A = exp(x - m), the denominator B = sum A, and the partial
+    output o = (A . v) / B.  A row with no admissible key in the subset
+    (possible under the causal mask) gets m = -inf, B = 0 and o = 0.
+    Returns (o [S,d], m [S], B [S]).
+    """
+    q_bh, k_bh, v_bh = _f64(q_bh), _f64(k_bh), _f64(v_bh)
+    key_idx = np.asarray(key_idx, dtype=np.int64)
+    n = q_bh.shape[0]
+    x = scores(q_bh, k_bh[key_idx], scale)               # [S, |subset|]
+    if causal:
+        x = np.where(key_idx[None, :] <= np.arange(n)[:, None], x, -np.inf)
+    m = x.max(axis=1)
+    o = np.zeros((n, v_bh.shape[1]))
+    Bsum = np.zeros(n)
+    ok = np.isfinite(m)
+    A = np.exp(x[ok] - m[ok][:, None])
+    Bsum[ok] = A.sum(axis=1)
+    o[ok] = (A @ v_bh[key_idx]) / Bsum[ok][:, None]
+    return o, m, Bsum
+
+
+def merge_two_halves(o_l, m_l, B_l, o_r, m_r, B_r):
+    """Merge two partial attentions over disjoint key sets.
+
+    Same page as ``partial_attention``: with m = max(m_l, m_r),
+      B = e^(m_l - m) B_l + e^(m_r - m) B_r
+      o = (B_l e^(m_l - m) o_l + B_r e^(m_r - m) o_r) / B
+    The merged logsumexp is L = m + log B.  Returns (o, m, B, L).
+    """
+    m = np.maximum(m_l, m_r)
+    wl = np.where(np.isfinite(m_l), np.exp(m_l - m), 0.0) * B_l
+    wr = np.where(np.isfinite(m_r), np.exp(m_r - m), 0.0) * B_r
+    Bm = wl + wr
+    o = (wl[:, None] * o_l + wr[:, None] * o_r) / Bm[:, None]
+    return o, m, Bm, m + np.log(Bm)

@@ -1,0 +1,261 @@
+"""Pins that tie the fp64 oracle to facts other than itself (CPU only).
+
+Each test checks the oracle against a hand-worked example, a closed form, an
+invariant of exact softmax attention, finite differences or an independent
+brute-force evaluation in plain Python.  Together they catch a dropped term,
+a wrong sign, a transposed operand, a wrong mask direction or a misplaced
+scale anywhere in the oracle.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(seed, *shape):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- hand-worked example
+@pytest.mark.parametrize("causal", [False, True])
+def test_hand_worked_two_rows(causal):
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_2x1.json")))
+    p = g["params"]
+    env = dict(c=p["c"], a=p["a"], b=p["b"], E1=math.exp(p["c"]), E2=math.exp(2 * p["c"]),
+               log=math.log)
+    ev = lambda xs: np.array([eval(x, {"__builtins__": {}}, env) if isinstance(x, str) else x
+                              for x in xs])
+    q = np.array(g["Q"])[None, None]
+    k = np.array(g["K"])[None, None]
+    v = np.array(g["V"])[None, None]
+    do = ev(g["dO"]).reshape(1, 1, 2, 1)
+    exp = g["causal" if causal else "noncausal"]
+    O, L = oracle.attention_fwd(q, k, v, causal, p["c"])
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal, p["c"])
+    np.testing.assert_allclose(O[0, 0, :, 0], ev(exp["O"]), rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(L[0, 0], ev(exp["L"]), rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(dv[0, 0, :, 0], ev(exp["dV"]), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dq[0, 0, :, 0], ev(exp["dQ"]), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dk[0, 0, :, 0], ev(exp["dK"]), rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- closed forms
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_gives_v(causal):
+    """S = 1: the only weight is 1, so O = V, L = q.k*scale, dV = dO, dQ = dK = 0."""
+    q, k, v, do = (rnd(s, 2, 3, 1, 8) for s in range(4))
+    sc = 0.37
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    np.testing.assert_allclose(O, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L, sc * np.sum(q * k, -1), rtol=1e-14, atol=1e-15)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal, sc)
+    np.testing.assert_allclose(dv, do, rtol=0, atol=1e-15)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+
+
+def test_zero_queries_causal_prefix_mean():
+    """Q = 0, causal: P_ij = 1/(i+1) for j <= i, so O_i is the prefix mean of V,
+    L_i = log(i+1), dK = 0, dV_j = sum_{i>=j} dO_i/(i+1), and
+    dQ_i = scale * sum_{j<=i} (dO_i.V_j - dO_i.O_i) K_j / (i+1)."""
+    S, d, sc = 9, 5, 0.41
+    q = np.zeros((1, 1, S, d))
+    k, v, do = rnd(10, 1, 1, S, d), rnd(11, 1, 1, S, d), rnd(12, 1, 1, S, d)
+    O, L = oracle.attention_fwd(q, k, v, True, sc)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, True, sc)
+    V, K, dO = v[0, 0], k[0, 0], do[0, 0]
+    for i in range(S):
+        mean = sum(V[j] for j in range(i + 1)) / (i + 1)
+        np.testing.assert_allclose(O[0, 0, i], mean, rtol=1e-14, atol=1e-14)
+        assert abs(L[0, 0, i] - math.log(i + 1)) < 1e-14
+        dqi = sum((dO[i] @ V[j] - dO[i] @ mean) * K[j] for j in range(i + 1)) * sc / (i + 1)
+        np.testing.assert_allclose(dq[0, 0, i], dqi, rtol=1e-12, atol=1e-13)
+    for j in range(S):
+        dvj = sum(dO[i] / (i + 1) for i in range(j, S))
+        np.testing.assert_allclose(dv[0, 0, j], dvj, rtol=1e-13, atol=1e-14)
+    assert np.abs(dk).max() == 0.0
+
+
+def test_zero_queries_noncausal_mean():
+    S, d = 7, 3
+    q = np.zeros((1, 2, S, d))
+    k, v, do = rnd(20, 1, 2, S, d), rnd(21, 1, 2, S, d), rnd(22, 1, 2, S, d)
+    O, L = oracle.attention_fwd(q, k, v, False, 0.9)
+    np.testing.assert_allclose(O, np.broadcast_to(v.mean(2, keepdims=True), O.shape), atol=1e-14)
+    np.testing.assert_allclose(L, math.log(S), atol=1e-14)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, False, 0.9)
+    np.testing.assert_allclose(dv, np.broadcast_to(do.sum(2, keepdims=True) / S, dv.shape),
+                               atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_value_rows(causal):
+    """V_j = v for every j: O = v and dP_ij = dO_i.v = D_i, so dS = 0 and dQ = dK = 0."""
+    S, d = 8, 4
+    q, k, do = rnd(30, 1, 1, S, d), rnd(31, 1, 1, S, d), rnd(32, 1, 1, S, d)
+    v = np.broadcast_to(rnd(33, d), (1, 1, S, d)).copy()
+    O, _ = oracle.attention_fwd(q, k, v, causal, 0.5)
+    np.testing.assert_allclose(O, v, atol=1e-14)
+    dq, dk, _ = oracle.attention_bwd(q, k, v, do, causal, 0.5)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+
+
+# ---------------------------------------------------------------- brute force
+def _brute_fwd(Q, K, V, causal, sc):
+    S, d = len(Q), len(Q[0])
+    O, L = [], []
+    for i in range(S):
+        js = [j for j in range(S) if (j <= i or not causal)]
+        s = {j: sc * sum(Q[i][t] * K[j][t] for t in range(d)) for j in js}
+        den = sum(math.exp(s[j]) for j in js)
+        O.append([sum(math.exp(s[j]) / den * V[j][t] for j in js) for t in range(d)])
+        L.append(math.log(den))
+    return np.array(O), np.array(L)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_matches_brute_force_loops(causal):
+    S, d, sc = 6, 3, 0.7
+    q, k, v = rnd(40, 1, 1, S, d), rnd(41, 1, 1, S, d), rnd(42, 1, 1, S, d)
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    Ob, Lb = _brute_fwd(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), causal, sc)
+    np.testing.assert_allclose(O[0, 0], Ob, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(L[0, 0], Lb, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dsoftmax_jacobian_brute_force(causal):
+    """Eq. 9 with the Jacobian diag(P_i) - P_i P_i^T built explicitly per row."""
+    S, d, sc = 5, 3, 0.8
+    q, k, v, do = (rnd(50 + s, 1, 1, S, d) for s in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal, sc)
+    Q, K, V, dO = q[0, 0], k[0, 0], v[0, 0], do[0, 0]
+    Sm = sc * Q @ K.T
+    if causal:
+        Sm = np.where(np.tril(np.ones((S, S), bool)), Sm, -np.inf)
+    P = np.exp(Sm - Sm.max(1, keepdims=True))
+    P /= P.sum(1, keepdims=True)
+    dP = dO @ V.T
+    dS = np.stack([(np.diag(P[i]) - np.outer(P[i], P[i])) @ dP[i] for i in range(S)])
+    np.testing.assert_allclose(dq[0, 0], sc * dS @ K, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dk[0, 0], sc * dS.T @ Q, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dv[0, 0], P.T @ dO, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_finite_differences(causal):
+    """Central differences of loss = sum(W * O) w.r.t. Q, K, V (fp64, h = 1e-6)."""
+    S, d, sc, h = 5, 3, 0.6, 1e-6
+    q, k, v, w = (rnd(60 + s, 1, 1, S, d) for s in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, w, causal, sc)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(w * oracle.attention_fwd(q_, k_, v_, causal, sc)[0]))
+
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        num = np.zeros((S, d))
+        for i in range(S):
+            for t in range(d):
+                args_p = [q.copy(), k.copy(), v.copy()]
+                args_m = [q.copy(), k.copy(), v.copy()]
+                args_p[which][0, 0, i, t] += h
+                args_m[which][0, 0, i, t] -= h
+                num[i, t] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(grad[0, 0], num, rtol=1e-6, atol=1e-8)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(causal):
+    """K_j += u for all j adds scale*Q_i.u to every score of row i: P, O, dQ, dK, dV
+    are unchanged and L_i moves by scale*Q_i.u."""
+    S, d, sc = 8, 4, 0.45
+    q, k, v, do = (rnd(70 + s, 1, 2, S, d) for s in range(4))
+    u = rnd(74, d)
+    O1, L1 = oracle.attention_fwd(q, k, v, causal, sc)
+    O2, L2 = oracle.attention_fwd(q, k + u, v, causal, sc)
+    np.testing.assert_allclose(O2, O1, atol=1e-13)
+    np.testing.assert_allclose(L2 - L1, sc * q @ u, atol=1e-13)
+    g1 = oracle.attention_bwd(q, k, v, do, causal, sc)
+    g2 = oracle.attention_bwd(q, k + u, v, do, causal, sc)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_key_permutation_invariance_noncausal():
+    S, d = 8, 4
+    q, k, v, do = (rnd(80 + s, 1, 1, S, d) for s in range(4))
+    perm = np.random.default_rng(84).permutation(S)
+    O1, L1 = oracle.attention_fwd(q, k, v, False, 0.5)
+    O2, L2 = oracle.attention_fwd(q, k[:, :, perm], v[:, :, perm], False, 0.5)
+    np.testing.assert_allclose(O2, O1, atol=1e-14)
+    np.testing.assert_allclose(L2, L1, atol=1e-14)
+    _, dk1, dv1 = oracle.attention_bwd(q, k, v, do, False, 0.5)
+    _, dk2, dv2 = oracle.attention_bwd(q, k[:, :, perm], v[:, :, perm], do, False, 0.5)
+    np.testing.assert_allclose(dk2, dk1[:, :, perm], atol=1e-13)
+    np.testing.assert_allclose(dv2, dv1[:, :, perm], atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_sums_and_d_identity(causal):
+    """Rows of dS sum to 0, hence sum_j dK_j = 0; and D = rowsum(O*dO) equals
+    rowsum(P*dP) (handout, backward pass with recomputation)."""
+    S, d, sc = 10, 6, 0.3
+    q, k, v, do = (rnd(90 + s, 1, 1, S, d) for s in range(4))
+    O, _ = oracle.attention_fwd(q, k, v, causal, sc)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal, sc)
+    np.testing.assert_allclose(dk.sum(2), 0.0, atol=1e-13)
+    D = oracle.rowsum_o_do(O, do)[0, 0]
+    Q, K, V, dO = q[0, 0], k[0, 0], v[0, 0], do[0, 0]
+    for i in range(S):
+        js = range(i + 1) if causal else range(S)
+        s = [sc * (Q[i] @ K[j]) for j in js]
+        den = sum(math.exp(x) for x in s)
+        val = sum(math.exp(x) / den * (dO[i] @ V[j]) for x, j in zip(s, js))
+        assert abs(val - D[i]) < 1e-12
+
+
+# ---------------------------------------------------------------- two-half merge
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("split", [1, 4, 7])
+def test_two_half_merge_equals_full(causal, split):
+    S, d, sc = 8, 4, 0.55
+    q, k, v = (rnd(100 + s, 1, 1, S, d)[0, 0] for s in range(3))
+    O, L = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], causal, sc)
+    ol, ml, bl = oracle.partial_attention(q, k, v, np.arange(split), causal, sc)
+    orr, mr, br = oracle.partial_attention(q, k, v, np.arange(split, S), causal, sc)
+    om, m, Bm, Lm = oracle.merge_two_halves(ol, ml, bl, orr, mr, br)
+    np.testing.assert_allclose(om, O[0, 0], atol=1e-14)
+    np.testing.assert_allclose(Lm, L[0, 0], atol=1e-14)
+
+
+def test_sampled_rows_match_full():
+    S, d = 12, 4
+    q, k, v = (rnd(110 + s, 1, 1, S, d) for s in range(3))
+    for causal in (False, True):
+        O, L = oracle.attention_fwd(q, k, v, causal, 0.5)
+        rows = [0, 5, 11]
+        Or, Lr = oracle.attention_fwd_rows(q[0, 0], k[0, 0], v[0, 0], rows, causal, 0.5)
+        np.testing.assert_allclose(Or, O[0, 0, rows], atol=1e-15)
+        np.testing.assert_allclose(Lr, L[0, 0, rows], atol=1e-15)
+
+
+# ---------------------------------------------------------------- library cross-check (extra)
+@pytest.mark.parametrize("causal", [False, True])
+def test_torch_sdpa_fp64_cross_check(causal):
+    torch = pytest.importorskip("torch")
+    S, d, sc = 16, 8, 0.25
+    q, k, v, do = (rnd(120 + s, 2, 2, S, d) for s in range(4))
+    O, _ = oracle.attention_fwd(q, k, v, causal, sc)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal, sc)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=sc)
+    to.backward(torch.tensor(do))
+    np.testing.assert_allclose(O, to.detach().numpy(), atol=1e-12)
+    for a, t in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-12)
