@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Benchmark of exact attention (FlashAttention-2 style) on one GB300.
+
+One step = one forward plus one backward pass of causal bf16 attention over
+the B4 H12 S1024 d64 small-LM workload (``c2``), inputs resident in HBM.
+Prints ONE JSON line (rank 0):
+
+  value        fwd+bwd TFLOP/s, FLOPs = 3.5 * 4*B*H*S^2*d * 1/2 (causal), whole job
+  e2e          the same metric through the C-ABI with pinned host buffers:
+               H2D of q, k, v, dO and D2H of o, lse, dq, dk, dv inside the timing
+  roofline     the dominant kernel's algorithmic TFLOP/s against the measured peak
+  cpu_baseline the fp64 oracle timed on this host's cores on a bounded sample
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+        [--workload c2|c3|c4|sweep:S:d]
+Under torchrun every rank runs its own copy of the workload (independent
+(batch, head) slices: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from seeded_inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20          # > the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def workload(name: str) -> Workload:
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name.startswith("sweep:"):           # sweep:S:d[:dtype]
+        parts = name.split(":")
+        S, d = int(parts[1]), int(parts[2])
+        dt = parts[3] if len(parts) > 3 else "bf16"
+        return Workload(name, 1, 16, S, d, dt, (True,), 1.0, 4242)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def flops_fwd(w: Workload, causal=True) -> float:
+    f = 4.0 * w.B * w.H * w.S * w.S * w.d
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a window."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for (_, r) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(w: Workload, seconds: float):
+    """Time the fp64 oracle (fwd + standard bwd) on whole (b, h) slices of the
+    workload until `seconds` have passed; returns (TFLOP/s on the bench's FLOP
+    count, slices done, elapsed seconds, threads)."""
+    import numpy as np
+    import oracle
+    q, k, v, do = make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed, w.qkv_scale)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    per_slice = 3.5 * flops_fwd(Workload("s", 1, 1, w.S, w.d, w.dtype, (True,)), True)
+    done, t0 = 0, time.perf_counter()
+    slices = [(b, h) for b in range(w.B) for h in range(w.H)]
+    while True:
+        b, h = slices[done % len(slices)]
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        oracle.attention_fwd(sl(q), sl(k), sl(v), True, w.scale)
+        oracle.attention_bwd(sl(q), sl(k), sl(v), sl(do), True, w.scale)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 4 * len(slices):
+            break
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "0")) or len(os.sched_getaffinity(0))
+    return per_slice * done / el / 1e12, done, el, threads
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = workload(args.workload)
+    import numpy as np  # noqa: F401
+    import oracle
+    q, k, v, do = make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed, w.qkv_scale)
+    f64 = lambda t: t.to(torch.float64).numpy()
+    per_slice = 3.5 * flops_fwd(Workload("s", 1, 1, w.S, w.d, w.dtype, (True,)), True)
+    slices = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def step(i):
+        b, h = slices[i % len(slices)]
+        sl = lambda t: f64(t[b:b + 1, h:h + 1])
+        oracle.attention_fwd(sl(q), sl(k), sl(v), True, w.scale)
+        oracle.attention_bwd(sl(q), sl(k), sl(v), sl(do), True, w.scale)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = per_slice * args.steps / el / 1e12
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", "0")) or len(os.sched_getaffinity(0))
+    sample = f"one (b,h) slice of {w.name} (S={w.S}, d={w.d}) per step: fp64 fwd + standard bwd"
+    print(json.dumps({
+        "impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16, causal)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
+                   "sample": "one (b,h) slice per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def load_traffic(kernel_name: str, workload_name: str):
+    """DRAM bytes per launch from a committed ncu summary, only if the kernel
+    source it was taken from is unchanged."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        j = json.load(open(p))
+        ent = j.get(kernel_name, {}).get(workload_name)
+        if not ent:
+            return None
+        src = os.path.join(ROOT, ent["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["dram_bytes_per_launch"] if sha == ent["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+def run_ours(args, world, rank, local):
+    import exact_attention_fa2_gb300 as fa
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    w = workload(args.workload)
+    causal = True
+    scale = w.scale
+    q, k, v, do = make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed + 7919 * rank, w.qkv_scale)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    dqd, dkd, dvd = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(fa.bwd_workspace_size(w.B, w.H, w.S, w.d, qd.dtype), device=dev, dtype=torch.uint8)
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fwd(qd, kd, vd, causal, scale, out=od, lse=lsed)
+        fa.bwd(qd, kd, vd, od, dod, lsed, causal, scale, workspace=ws, out=(dqd, dkd, dvd))
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    fa.check_status()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    fa.profile_read()                      # drop anything recorded so far
+    fa.profile_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()                       # L2 flush between timed steps (outside the events)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    fa.profile_enable(False)
+    prof = fa.profile_read()
+    fa.check_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world)
+
+    # End to end through the public API with pinned host buffers.
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    e2e_steps = max(5, min(args.steps, 50))
+
+    def e2e_step():
+        for hsrc, ddst in ((hq, qd), (hk, kd), (hv, vd), (hdo, dod)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for dsrc, hdst in ((od, ho), (lsed, hlse), (dqd, hdq), (dkd, hdk), (dvd, hdv)):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    barrier(world)
+    e2e_ms_step = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    f_fwd = flops_fwd(w, causal)
+    step_flops = 3.5 * f_fwd
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    e2e_value = world * step_flops / (e2e_ms_step * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # Dominant kernel: the one with the largest share of timed device time.
+    kern_flops = {"fwd": f_fwd, "bwd_main": 2.5 * f_fwd}
+    shares = {k: v[0] for k, v in prof.items()}
+    dom = max(("fwd", "bwd_main"), key=lambda k: shares[k])
+    dom_ms, dom_n = prof[dom]
+    achieved = kern_flops[dom] / (dom_ms / max(dom_n, 1) * 1e-3) / 1e12 if dom_n else None
+    peak = peaks["bf16_tflops"]
+    kernel_names = {"fwd": "fa_fwd_kernel", "bwd_main": "fa_bwd_kernel"}
+    traffic = load_traffic(kernel_names[dom], w.name)
+    per = lambda k: (prof[k][0] / max(prof[k][1], 1)) if prof[k][1] else None
+    fwd_ms, bwd_ms = per("fwd"), per("bwd_main")
+    total_kernel_ms = sum(v[0] for v in prof.values())
+
+    line = {
+        "metric": "attention fwd+bwd TFLOP/s (bf16, causal)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
+                   "B": w.B, "H": w.H, "S": w.S, "d": w.d, "causal": causal,
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "parallelism": f"replica per GPU x{world} (independent heads, no collective)"},
+        "frac_of_peak": {"burst": value / peaks["bf16_tflops"],
+                         "sustained": value / peaks["bf16_tflops_sustained"], "peaks": peaks["source"]},
+        "kernels": {"fwd_ms": fwd_ms, "bwd_main_ms": bwd_ms,
+                    "bwd_preprocess_ms": per("bwd_preprocess"), "dq_convert_ms": per("dq_convert"),
+                    "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
+                    "bwd_tflops": 2.5 * f_fwd / ((ms_per_step - fwd_ms) * 1e-3) / 1e12 if fwd_ms else None,
+                    "shares": {k: (v[0] / total_kernel_ms if total_kernel_ms else None) for k, v in prof.items()}},
+        "roofline": {"kernel": kernel_names[dom], "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(v[1] for v in prof.values()),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_cpu, n_sl, el, thr = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{n_sl} (b,h) slices of {w.name} (of {w.B * w.H}), fp64 fwd + "
+                                          f"standard bwd, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,222 @@
+"""Python binding of the GB300 exact-attention library (``libfa_gb300.so``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/fa_gb300.h``.  PyTorch supplies
+device memory and the current stream.  There is no CPU fallback: if the
+library has not been built, or the tensors are not on a CUDA device, the calls
+raise.
+
+Layout: q, k, v, o, dO, dq, dk, dv are contiguous [B, H, S, d] tensors
+(bfloat16 or float32); lse is [B, H, S] float32 (natural log).
+
+The autograd contract follows the "CS336 Assignment 2: Systems" FlashAttention-2
+section and the handout's problem flash_forward: forward(Q, K, V, is_causal)
+returns O and saves L, Q, K, V, O; backward(dO) returns dQ, dK, dV.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "FAError", "library_path", "load_library", "fa_fwd", "fa_bwd", "fwd", "bwd",
+    "bwd_workspace_size", "check_status", "attention", "FlashAttention", "version",
+    "FA_BF16", "FA_FP32", "profile_enable", "profile_read",
+]
+
+FA_BF16 = 0
+FA_FP32 = 1
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED", -3: "FA_ERR_MISALIGNED",
+    -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_CUDA", -6: "FA_ERR_DEVICE_TIMEOUT", -7: "FA_ERR_DEVICE_BOUNDS",
+}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_FILE = os.path.join(_PKG, "libfa_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_FILE
+
+
+def load_library():
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_FILE):
+            raise RuntimeError(
+                f"{_LIB_FILE} is missing: build it with `python -m exact_attention_fa2_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(_LIB_FILE)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_get_last_error.argtypes = []
+        lib.fa_get_last_error.restype = ctypes.c_char_p
+        lib.fa_check_status.argtypes = [vp]
+        lib.fa_check_status.restype = i
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i
+        lib.fa_profile_enable.argtypes = [i]
+        lib.fa_profile_enable.restype = i
+        lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+        lib.fa_profile_read.restype = i
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != FA_OK:
+        raise FAError(rc, load_library().fa_get_last_error().decode(errors="replace"))
+
+
+def version() -> int:
+    return load_library().fa_version()
+
+
+PROFILE_KINDS = ("fwd", "bwd_preprocess", "bwd_main", "dq_convert")
+
+
+def profile_enable(on: bool = True):
+    """Start or stop per-kernel CUDA-event timing inside the library."""
+    _check(load_library().fa_profile_enable(1 if on else 0))
+
+
+def profile_read():
+    """{kind: (total_ms, launches)} for the kernels timed since the last read."""
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_int * 4)()
+    _check(load_library().fa_profile_read(ms, n))
+    return {k: (ms[i], n[i]) for i, k in enumerate(PROFILE_KINDS)}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_qkv(*ts):
+    q = ts[0]
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device (there is no CPU fallback)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, S, d]")
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("q, k, v (and o, dO) must share shape, dtype and device")
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, S, d] tensors")
+
+
+def fa_fwd(q, k, v, o, lse, B, H, S, d, causal, scale, dtype, stream) -> int:
+    """Raw C-ABI call on device pointers (ints or ctypes pointers); returns the status."""
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, S, d, int(causal), float(scale), dtype, stream)
+
+
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, ws, ws_bytes, B, H, S, d, causal, scale, dtype, stream) -> int:
+    """Raw C-ABI call on device pointers; returns the status."""
+    return load_library().fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, ws, ws_bytes, B, H, S, d,
+                                 int(causal), float(scale), dtype, stream)
+
+
+def bwd_workspace_size(B: int, H: int, S: int, d: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (FA_BF16 if dtype == torch.bfloat16 else FA_FP32)
+    return int(load_library().fa_bwd_workspace_size(B, H, S, d, code))
+
+
+def check_status(stream=None):
+    """Synchronise the stream and raise if a kernel reported a device-side error."""
+    _check(load_library().fa_check_status(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def fwd(q, k, v, causal: bool = False, scale=None, out=None, lse=None, stream=None):
+    """Forward pass; returns (o, lse)."""
+    _check_qkv(q, k, v)
+    B, H, S, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, d, causal, scale,
+                    _dtype_code(q), ctypes.c_void_p(_stream_handle(stream)))
+    _check(rc)
+    return o, lse
+
+
+def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, stream=None,
+        out=None):
+    """Backward pass; returns (dq, dk, dv).  ``workspace`` (uint8, >= the size
+    reported by bwd_workspace_size) is allocated here when not given."""
+    _check_qkv(q, k, v, o, do)
+    B, H, S, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code = _dtype_code(q)
+    need = bwd_workspace_size(B, H, S, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    with torch.cuda.device(q.device):
+        rc = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                    _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                    B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
+    _check(rc)
+    return dq, dk, dv
+
+
+class FlashAttention(torch.autograd.Function):
+    """O = softmax(Q K^T * scale) V with the recompute backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, is_causal=False, scale=None):
+        o, lse = fwd(q, k, v, is_causal, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.is_causal = bool(is_causal)
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, ctx.is_causal, ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale=None):
+    return FlashAttention.apply(q, k, v, causal, scale)

@@ -1,0 +1,235 @@
+// fa_api.cu - the C ABI (include/fa_gb300.h): argument checks, workspace
+// layout, kernel selection and error reporting.  No device memory is
+// allocated here; the only device state is one status word per device that
+// kernels set when a bounded wait runs out or an index check fails.
+
+#include "fa_gb300.h"
+#include "fa_common.cuh"
+#include "fa_launch.h"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+namespace {
+
+__device__ unsigned int g_status_word;
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Device address of this device's status word (looked up once per device).
+int status_ptr(unsigned int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return FA_OK;
+}
+
+bool supported_d(int d) {
+    return d == 16 || d == 32 || d == 64 || d == 80 || d == 96 || d == 128;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks shared by forward and backward.  Returns FA_OK, an error code, or 1
+// for a valid empty problem (nothing to launch).
+int check_sizes(int B, int H, int S, int d, float scale, int dtype) {
+    if (B < 0 || H < 0 || S < 0)
+        return fail(FA_ERR_INVALID_ARG, "negative size: B=%d H=%d S=%d", B, H, S);
+    if (dtype != FA_BF16 && dtype != FA_FP32)
+        return fail(FA_ERR_UNSUPPORTED, "dtype %d is not FA_BF16 or FA_FP32", dtype);
+    if (!supported_d(d))
+        return fail(FA_ERR_UNSUPPORTED, "head dim %d not in {16,32,64,80,96,128}", d);
+    if (!std::isfinite(scale))
+        return fail(FA_ERR_INVALID_ARG, "scale is not finite");
+    const long long n = (long long)B * H * S * d;
+    if (n >= (1LL << 31))
+        return fail(FA_ERR_UNSUPPORTED, "B*H*S*d = %lld elements exceeds 2^31-1", n);
+    if ((long long)B * H > 65535LL)
+        return fail(FA_ERR_UNSUPPORTED, "B*H = %lld exceeds 65535", (long long)B * H);
+    if ((long long)B * H * S == 0) return 1;
+    return FA_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+    if (!p) return fail(FA_ERR_INVALID_ARG, "%s is null", name);
+    if (!aligned16(p)) return fail(FA_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    return FA_OK;
+}
+
+// ---- optional kernel timing (fa_profile_enable / fa_profile_read)
+enum { PROF_FWD = 0, PROF_PRE = 1, PROF_BWD = 2, PROF_CONV = 3, PROF_KINDS = 4 };
+struct ProfRec { cudaEvent_t a, b; int kind; };
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_ev_pool;
+
+cudaEvent_t prof_event() {
+    if (!g_ev_pool.empty()) {
+        cudaEvent_t e = g_ev_pool.back();
+        g_ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Runs `launch` on `stream`, bracketed by timing events when profiling is on.
+template <typename F>
+cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        if (g_prof_on) { a = prof_event(); b = prof_event(); }
+    }
+    if (a && b) cudaEventRecord(a, stream);
+    cudaError_t e = launch();
+    if (a && b) {
+        cudaEventRecord(b, stream);
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_prof_pending.push_back({a, b, kind});
+    }
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = on != 0;
+    return FA_OK;
+}
+
+int fa_profile_read(double* ms, int* launches) {
+    if (!ms || !launches) return fail(FA_ERR_INVALID_ARG, "null output array");
+    std::vector<ProfRec> recs;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        recs.swap(g_prof_pending);
+    }
+    int rc = FA_OK;
+    for (const ProfRec& r : recs) {
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+        if (e != cudaSuccess) { rc = cuda_fail(e, "profile event"); continue; }
+        ms[r.kind] += t;
+        launches[r.kind] += 1;
+    }
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (const ProfRec& r : recs) { g_ev_pool.push_back(r.a); g_ev_pool.push_back(r.b); }
+    return rc;
+}
+
+
+int fa_version(void) { return 100; }
+
+const char* fa_get_last_error(void) { return g_err; }
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(B, H, S, d, scale, dtype);
+    if (rc == 1) return FA_OK;
+    if (rc) return rc;
+    if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+        (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")))
+        return rc;
+    fa::FwdArgs a{q, k, v, o, lse, B, H, S, d, causal ? 1 : 0, scale, dtype,
+                  static_cast<cudaStream_t>(stream), nullptr};
+    if ((rc = status_ptr(&a.status))) return rc;
+    cudaError_t e = timed(PROF_FWD, a.stream, [&] { return fa::launch_fwd_simt(a); });
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype) {
+    if (B <= 0 || H <= 0 || S <= 0 || !supported_d(d) || (dtype != FA_BF16 && dtype != FA_FP32))
+        return 0;
+    const size_t rows = (size_t)B * H * S;
+    return align_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv,
+           void* workspace, size_t workspace_bytes,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(B, H, S, d, scale, dtype);
+    if (rc == 1) return FA_OK;
+    if (rc) return rc;
+    if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+        (rc = check_ptr(o, "o")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(lse, "lse")) ||
+        (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+        return rc;
+    const size_t need = fa_bwd_workspace_size(B, H, S, d, dtype);
+    if (!workspace || workspace_bytes < need)
+        return fail(FA_ERR_WORKSPACE, "workspace %p of %zu bytes, need %zu", workspace, workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    const size_t rows = (size_t)B * H * S;
+    float* Dvec = static_cast<float*>(workspace);
+    float* dQacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * sizeof(float), 256));
+    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, Dvec, dQacc, B, H, S, d, causal ? 1 : 0, scale,
+                  dtype, static_cast<cudaStream_t>(stream), nullptr};
+    if ((rc = status_ptr(&a.status))) return rc;
+    cudaError_t e = timed(PROF_PRE, a.stream, [&] { return fa::launch_bwd_preprocess(a); });
+    if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+    e = timed(PROF_BWD, a.stream, [&] { return fa::launch_bwd_simt(a); });
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    e = timed(PROF_CONV, a.stream, [&] { return fa::launch_dq_convert(a); });
+    if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
+    return FA_OK;
+}
+
+int fa_check_status(void* stream) {
+    g_err[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (word == 0) return FA_OK;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    if (word & FA_DEV_STATUS_TIMEOUT)
+        return fail(FA_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (status 0x%x)", word);
+    return fail(FA_ERR_DEVICE_BOUNDS, "a kernel caught an out-of-range index (status 0x%x)", word);
+}
+
+}  // extern "C"

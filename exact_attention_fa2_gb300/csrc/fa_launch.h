@@ -1,0 +1,57 @@
+// fa_launch.h - host-side launch interface between the C ABI and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace fa {
+
+enum { DT_BF16 = 0, DT_FP32 = 1 };
+
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int B, H, S, d;
+    int causal;
+    float scale;
+    int dtype;
+    cudaStream_t stream;
+    unsigned int* status;   // device status word (timeouts, index checks)
+};
+
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* dO;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* Dvec;            // [B*H*S] fp32, inside the workspace
+    float* dQacc;           // [B*H*S*d] fp32, inside the workspace
+    int B, H, S, d;
+    int causal;
+    float scale;
+    int dtype;
+    cudaStream_t stream;
+    unsigned int* status;
+};
+
+// fp32 (and generic) FMA-pipe kernels.
+cudaError_t launch_fwd_simt(const FwdArgs& a);
+cudaError_t launch_bwd_simt(const BwdArgs& a);
+
+// Backward helpers: D = rowsum(O*dO) plus zeroing of dQacc; dQacc -> dq.
+cudaError_t launch_bwd_preprocess(const BwdArgs& a);
+cudaError_t launch_dq_convert(const BwdArgs& a);
+
+// bf16 tensor-core (tcgen05) kernels.
+cudaError_t launch_fwd_tc(const FwdArgs& a);
+cudaError_t launch_bwd_tc(const BwdArgs& a);
+
+}  // namespace fa

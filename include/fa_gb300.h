@@ -1,0 +1,139 @@
+/*
+ * fa_gb300.h - C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention
+ *     O = softmax(Q K^T * scale) V,   L_i = log sum_j exp((Q K^T * scale)_ij)
+ * in the FlashAttention-2 manner (tiled over keys with an online softmax; the
+ * S x S score matrix is never written to memory), and its recompute backward
+ * (dQ, dK, dV from Q, K, V, O, dO and L, using D = rowsum(O * dO)).
+ *
+ * Sources for the operations:
+ *   - "Stanford CS336 Assignment 2 (Systems)" handout, section 4
+ *     "FlashAttention-2": Eq. 4-6 (forward), Eq. 12 (logsumexp L), Eq. 13-19
+ *     (backward with recomputation and D), Algorithm 1 (tiled forward),
+ *     Algorithm 2 (tiled backward), problem flash_forward (c) (causal mask).
+ *   - "CS336 Assignment 2: Systems" blog, FlashAttention-2 section: the
+ *     autograd contract forward(Q, K, V, is_causal) -> O saving L, and
+ *     backward(dO) -> dQ, dK, dV.
+ *   - "Phase T14: fused Flash-Attention kernel - design document" (xtrain):
+ *     launch entry points over a C FFI and an fp32 logsumexp.
+ *
+ * Conventions shared by every entry point
+ *   Layout   q, k, v, o, dO, dq, dk, dv are contiguous [B, H, S, d] arrays of
+ *            the element type `dtype` (row-major, d fastest).  lse is a
+ *            contiguous [B, H, S] fp32 array holding the natural-log L.
+ *            Self-attention only: queries and keys share the length S.
+ *   Causal   causal != 0 keeps key j for query i only when j <= i
+ *            (top-left aligned, square).
+ *   Pointers every array argument is a DEVICE pointer of the current CUDA
+ *            device, 16-byte aligned.  `stream` is a cudaStream_t passed as
+ *            void* (NULL = the legacy default stream).  All work is enqueued
+ *            asynchronously on that stream; nothing is synchronised.
+ *   Ownership the caller allocates and owns every buffer, including the
+ *            backward workspace; the library allocates no device memory and
+ *            keeps only host-side state (cached kernel attributes).
+ *   Sizes    B, H, S >= 0 (a zero size is a valid empty problem and returns
+ *            FA_OK without launching); d in {16, 32, 64, 80, 96, 128};
+ *            B*H <= 65535 and B*H*S*d < 2^31 elements per array.  Any S >= 1 is accepted
+ *            (a ragged last tile is masked).
+ *   Errors   every call returns FA_OK (0) or a negative fa_status code and
+ *            never aborts or traps; fa_get_last_error() describes the last
+ *            failure of the calling thread.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_BF16 = 0,   /* bfloat16 storage, fp32 accumulation, tcgen05 tensor cores */
+    FA_FP32 = 1    /* fp32 storage and arithmetic on the FMA pipes (tight checks) */
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,     /* null pointer, negative size, non-finite scale */
+    FA_ERR_UNSUPPORTED = -2,     /* head dim or dtype outside the supported set, or too large */
+    FA_ERR_MISALIGNED = -3,      /* an array pointer is not 16-byte aligned */
+    FA_ERR_WORKSPACE = -4,       /* workspace null or smaller than fa_bwd_workspace_size() */
+    FA_ERR_CUDA = -5,            /* a CUDA runtime/driver call or a launch failed */
+    FA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up a bounded wait (reported by fa_check_status) */
+    FA_ERR_DEVICE_BOUNDS = -7    /* a kernel caught an out-of-range index (reported by fa_check_status) */
+} fa_status;
+
+/*
+ * Forward pass: handout Eq. 4-6 and Eq. 12, computed as in Algorithm 1.
+ *   q, k, v  [B,H,S,d] dtype, read only.
+ *   o        [B,H,S,d] dtype, fully overwritten with softmax(QK^T*scale)V,
+ *            rounded to nearest even from the fp32 accumulator.
+ *   lse      [B,H,S] fp32, fully overwritten with L (natural log).
+ *   scale    the score scale (1/sqrt(d) in the handout); any finite value.
+ * bf16 rounds the unnormalised probabilities to bf16 before the PV product
+ * (handout, flash_forward (b): cast P to V's dtype); fp32 keeps them fp32.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs.  The workspace holds, in order,
+ *   D      [B,H,S] fp32   D_i = rowsum(O * dO)_i (handout, "backward pass with
+ *                         recomputation"; Algorithm 2 step 2), written by fa_bwd;
+ *   (zero padding to a 256-byte boundary)
+ *   dQacc  [B,H,S,d] fp32 the dQ accumulator that the key-tile-outer kernel adds
+ *                         into with fp32 atomics, zeroed by fa_bwd itself.
+ * Returns 0 for invalid or empty sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype);
+
+/*
+ * Backward pass: handout Eq. 13-19 with Algorithm 2's key-tile-outer loop for
+ * dK and dV; dQ is reduced across key tiles with fp32 atomics into dQacc and
+ * converted to dtype at the end (its last bits may differ from run to run).
+ *   q, k, v, o, dO  [B,H,S,d] dtype, read only; o must be the fa_fwd output.
+ *   lse             [B,H,S] fp32 from fa_fwd, read only.
+ *   dq, dk, dv      [B,H,S,d] dtype, fully overwritten.
+ *   workspace       device buffer of >= fa_bwd_workspace_size() bytes, 256-byte
+ *                   aligned; contents on entry are ignored, D is left in it.
+ * Same B, H, S, d, causal, scale and dtype as the forward call.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv,
+           void* workspace, size_t workspace_bytes,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/* Message for the calling thread's last non-zero return ("" if none). */
+const char* fa_get_last_error(void);
+
+/*
+ * Synchronise `stream` and read, then clear, the current device's status word
+ * that kernels set when a bounded wait runs out or an index check fails.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_BOUNDS or FA_ERR_CUDA.
+ */
+int fa_check_status(void* stream);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int fa_version(void);
+
+/*
+ * Kernel timing for benchmarks (not needed to compute attention).  While
+ * enabled, every fa_fwd / fa_bwd call records a pair of CUDA events on its
+ * stream directly around each of its kernels.  fa_profile_read waits for the
+ * recorded events, adds their elapsed times since the previous read into
+ * ms[4] and the number of timed launches into launches[4], indexed by
+ *   0 = forward kernel, 1 = backward preprocess (D, dQacc zeroing),
+ *   2 = backward main kernel, 3 = dQ conversion,
+ * and forgets them.  Both return FA_OK or FA_ERR_CUDA / FA_ERR_INVALID_ARG.
+ * Events come from a host-side pool; no device memory is allocated.
+ */
+int fa_profile_enable(int on);
+int fa_profile_read(double* ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads and exports every declared symbol; the host
+side of the argument checks works without a GPU (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_fa2_gb300 as fa
+from exact_attention_fa2_gb300 import build as fabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_error",
+                 "fa_check_status", "fa_version"):
+        assert must in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_version(lib):
+    assert lib.fa_version() >= 100
+
+
+def test_workspace_size(lib):
+    n = fa.bwd_workspace_size(2, 3, 100, 64, fa.FA_BF16)
+    rows = 2 * 3 * 100
+    assert n == ((rows * 4 + 255) // 256) * 256 + rows * 64 * 4
+    assert fa.bwd_workspace_size(0, 3, 100, 64, fa.FA_BF16) == 0
+    assert fa.bwd_workspace_size(1, 1, 1, 48, fa.FA_BF16) == 0
+
+
+A = 1 << 20   # a fake, 16-byte aligned, never dereferenced address
+
+
+def call_fwd(B=1, H=1, S=128, d=64, causal=0, scale=0.125, dtype=0, q=A, k=A, v=A, o=A, lse=A):
+    return fa.fa_fwd(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(o),
+                     ctypes.c_void_p(lse), B, H, S, d, causal, scale, dtype, None)
+
+
+def test_argument_errors_need_no_gpu(lib):
+    assert call_fwd(B=-1) == -1
+    assert call_fwd(d=48) == -2
+    assert call_fwd(dtype=7) == -2
+    assert call_fwd(scale=float("nan")) == -1
+    assert call_fwd(q=0) == -1
+    assert call_fwd(k=A + 8) == -3
+    assert b"16-byte" in lib.fa_get_last_error()
+    assert call_fwd(B=1 << 12, H=1 << 12, S=1 << 10, d=128) == -2   # too many elements
+    # Empty problems are valid and launch nothing.
+    assert call_fwd(S=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert call_fwd(B=0) == 0
+
+
+def test_bwd_workspace_errors_need_no_gpu(lib):
+    P = ctypes.c_void_p(A)
+    rc = fa.fa_bwd(P, P, P, P, P, P, P, P, P, P, 16, 1, 1, 128, 64, 1, 0.125, 0, None)
+    assert rc == -4 and b"workspace" in lib.fa_get_last_error()
+    rc = fa.fa_bwd(P, P, P, P, P, P, P, P, P, ctypes.c_void_p(A + 16), 1 << 30, 1, 1, 128, 64, 1,
+                   0.125, 0, None)
+    assert rc == -3

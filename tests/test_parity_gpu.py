@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the fp64 oracle.
+
+Inputs are the seeded synthetic tensors of ``seeded_inputs``; the oracle sees
+the same values widened exactly to float64.  Small problems are compared
+element by element in full; full-size workloads are compared on sampled
+(batch, head) slices, each computed exactly by the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_fa2_gb300 as fa
+import oracle
+from seeded_inputs import WORKLOADS, make_inputs, make_workload_inputs, sweep_points
+from tests.helpers import TOL, assert_close, f64, oracle_head
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from exact_attention_fa2_gb300 import build
+    build.build()
+    fa.load_library()
+
+
+def run_gpu(q, k, v, do, causal, scale):
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal, scale)
+    B, H, S, d = q.shape
+    ws = torch.empty(fa.bwd_workspace_size(B, H, S, d, q.dtype), device=DEV, dtype=torch.uint8)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, causal, scale, workspace=ws)
+    fa.check_status()
+    rows = B * H * S
+    D = ws[: rows * 4].view(torch.float32).view(B, H, S)
+    return [t.cpu() for t in (o, lse, dq, dk, dv, D)]
+
+
+def check_heads(q, k, v, do, causal, scale, dtype, heads, res=None):
+    o, lse, dq, dk, dv, D = res if res is not None else run_gpu(q, k, v, do, causal, scale)
+    tol = TOL[dtype]
+    for (b, h) in heads:
+        O, L, rdq, rdk, rdv = oracle_head(q, k, v, do, b, h, causal, scale)
+        tag = f"[b={b},h={h},causal={causal}]"
+        assert_close("O" + tag, o[b, h], O, *tol["o"])
+        assert_close("L" + tag, lse[b, h], L, *tol["lse"])
+        assert_close("dQ" + tag, dq[b, h], rdq, *tol["grad"])
+        assert_close("dK" + tag, dk[b, h], rdk, *tol["grad"])
+        assert_close("dV" + tag, dv[b, h], rdv, *tol["grad"])
+        # D from the GPU's own stored O and the dO it was given.
+        Dref = oracle.rowsum_o_do(f64(o[b, h]), f64(do[b, h]))
+        assert_close("D" + tag, D[b, h], Dref, *tol["D"])
+
+
+def all_heads(B, H):
+    return [(b, h) for b in range(B) for h in range(H)]
+
+
+# ------------------------------------------------------------------ workloads
+@pytest.mark.parametrize("causal", [True, False])
+def test_c1_fp32_full(causal):
+    w = WORKLOADS["c1"]
+    q, k, v, do = make_workload_inputs(w)
+    check_heads(q, k, v, do, causal, w.scale, w.dtype, all_heads(w.B, w.H))
+
+
+def test_c2_bf16_causal_sampled_heads():
+    w = WORKLOADS["c2"]
+    q, k, v, do = make_workload_inputs(w)
+    check_heads(q, k, v, do, True, w.scale, w.dtype, [(0, 0), (1, 7), (3, 11)])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_c3_bf16_sampled_heads(causal):
+    w = WORKLOADS["c3"]
+    q, k, v, do = make_workload_inputs(w)
+    check_heads(q, k, v, do, causal, w.scale, w.dtype, [(0, 3), (3, 15)])
+
+
+def test_c4_bf16_d80_sampled_heads():
+    w = WORKLOADS["c4"]
+    q, k, v, do = make_workload_inputs(w)
+    check_heads(q, k, v, do, True, w.scale, w.dtype, [(0, 0), (2, 31)])
+
+
+SWEEP = [p for p in sweep_points(4096)]
+
+
+@pytest.mark.parametrize("w", SWEEP, ids=[p.name for p in SWEEP])
+def test_c5_sweep_point(w):
+    q, k, v, do = make_workload_inputs(w)
+    heads = [(0, 5)] if w.S >= 2048 else [(0, 0), (0, 15)]
+    check_heads(q, k, v, do, True, w.scale, w.dtype, heads)
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 80, 96, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_lengths_every_head_dim(dtype, d, causal):
+    # 333 = 2*128 + 77: several tiles and a ragged tail.
+    q, k, v, do = make_inputs(2, 2, 333, d, dtype, seed=7000 + d)
+    check_heads(q, k, v, do, causal, 1.0 / math.sqrt(d), dtype, all_heads(2, 2))
+
+
+@pytest.mark.parametrize("S", [1, 2, 17, 127, 128, 129, 255, 257])
+def test_short_and_boundary_lengths(S):
+    q, k, v, do = make_inputs(1, 3, S, 64, "bf16", seed=7100 + S)
+    check_heads(q, k, v, do, True, 0.125, "bf16", all_heads(1, 3))
+    q, k, v, do = make_inputs(1, 1, S, 64, "fp32", seed=7200 + S)
+    check_heads(q, k, v, do, False, 0.125, "fp32", all_heads(1, 1))
+
+
+def test_single_key_closed_form():
+    q, k, v, do = make_inputs(2, 4, 1, 128, "bf16", seed=7300)
+    o, lse, dq, dk, dv, _ = run_gpu(q, k, v, do, True, 0.1)
+    assert torch.equal(o, v)                       # the only weight is exactly 1
+    assert torch.equal(dv, do)
+    # dS = P (dP - D) is a difference of two fp32 sums of the same products.
+    assert dq.abs().max().item() < 1e-3 and dk.abs().max().item() < 1e-3
+    np.testing.assert_allclose(f64(lse), 0.1 * np.sum(f64(q) * f64(k), -1), atol=1e-3)
+
+
+def test_empty_problem():
+    z = torch.empty((2, 3, 0, 64), device=DEV, dtype=torch.bfloat16)
+    o, lse = fa.fwd(z, z, z, True)
+    assert o.shape == z.shape and lse.shape == (2, 3, 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_custom_scale(dtype):
+    q, k, v, do = make_inputs(1, 2, 200, 32, dtype, seed=7400)
+    check_heads(q, k, v, do, True, 0.37, dtype, all_heads(1, 2))
+
+
+def test_zero_queries_large_causal_closed_form():
+    """Q = 0 at a length the oracle cannot materialise: P_ij = 1/(i+1), so
+    O_i is the prefix mean of V, L_i = log(i+1), dK = 0 and
+    dV_j = sum_{i>=j} dO_i/(i+1)."""
+    B, H, S, d = 1, 2, 16384, 64
+    _, k, v, do = make_inputs(B, H, S, d, "bf16", seed=7500)
+    q = torch.zeros_like(k)
+    o, lse, dq, dk, dv, _ = run_gpu(q, k, v, do, True, 0.125)
+    V, dO = f64(v), f64(do)
+    n = np.arange(1, S + 1, dtype=np.float64)[:, None]
+    prefix_mean = np.cumsum(V, axis=2) / n
+    assert_close("O", o, prefix_mean, 2e-2, 2e-2)
+    assert_close("L", lse, np.broadcast_to(np.log(n[:, 0]), (B, H, S)), 1e-3, 0)
+    assert dk.abs().max().item() == 0.0
+    dv_ref = np.cumsum((dO / n)[:, :, ::-1], axis=2)[:, :, ::-1]
+    assert_close("dV", dv, dv_ref, 5e-2, 5e-2)
+
+
+def test_long_sequence_sampled_rows():
+    """Forward rows are independent: sampled rows of an S = 32768 problem are
+    exact in the oracle without the full score matrix."""
+    B, H, S, d = 1, 1, 32768, 128
+    q, k, v, _ = make_inputs(B, H, S, d, "bf16", seed=7600)
+    o, lse = fa.fwd(q.to(DEV), k.to(DEV), v.to(DEV), True)
+    fa.check_status()
+    rows = [0, 1, 127, 128, 4095, 20000, S - 1]
+    Or, Lr = oracle.attention_fwd_rows(f64(q[0, 0]), f64(k[0, 0]), f64(v[0, 0]), rows, True, 1 / math.sqrt(d))
+    assert_close("O rows", o[0, 0, rows].cpu(), Or, 2e-2, 2e-2)
+    assert_close("L rows", lse[0, 0, rows].cpu(), Lr, 1e-3, 0)
+
+
+def test_repeat_runs_deterministic_where_promised():
+    """O, L, dK, dV come out bit-identical on repeated runs; dQ (fp32 atomics)
+    may differ only in its last bits."""
+    q, k, v, do = make_inputs(2, 4, 1024, 64, "bf16", seed=7700)
+    r1 = run_gpu(q, k, v, do, True, 0.125)
+    r2 = run_gpu(q, k, v, do, True, 0.125)
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), r1, r2):
+        if name == "dq":
+            assert_close("dq repeat", a, b, 1e-2, 1e-2)
+        else:
+            assert torch.equal(a, b), name
+
+
+def test_autograd_function_matches_oracle():
+    q, k, v, do = make_inputs(1, 2, 256, 64, "bf16", seed=7800)
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    out = fa.attention(qd, kd, vd, causal=True)
+    out.backward(do.to(DEV))
+    for b, h in all_heads(1, 2):
+        O, L, rdq, rdk, rdv = oracle_head(q, k, v, do, b, h, True, 0.125)
+        assert_close("O", out[b, h].detach().cpu(), O, *TOL["bf16"]["o"])
+        assert_close("dQ", qd.grad[b, h].cpu(), rdq, *TOL["bf16"]["grad"])
+        assert_close("dK", kd.grad[b, h].cpu(), rdk, *TOL["bf16"]["grad"])
+        assert_close("dV", vd.grad[b, h].cpu(), rdv, *TOL["bf16"]["grad"])
+
+
+def test_device_errors_are_reported_not_raised_on_device():
+    x = torch.zeros((1, 1, 128, 64), device=DEV, dtype=torch.bfloat16)
+    bad = torch.zeros(128 * 64 + 1, device=DEV, dtype=torch.bfloat16)[1:].view(1, 1, 128, 64)
+    with pytest.raises(fa.FAError) as e:
+        fa.fwd(bad, x, x, True)
+    assert e.value.code == -3
+    fa.check_status()
