@@ -28,6 +28,8 @@ from .attention import (  # noqa: F401
     attention_fwd,
     attention_fwd_rows,
     attention_bwd,
+    attention_bwd_from_output,
+    round_to_storage,
     rowsum_o_do,
     partial_attention,
     merge_two_halves,

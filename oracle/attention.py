@@ -13,7 +13,8 @@ import numpy as np
 
 __all__ = [
     "scores", "causal_keep", "attention_fwd", "attention_fwd_rows", "attention_bwd",
-    "rowsum_o_do", "partial_attention", "merge_two_halves",
+    "attention_bwd_from_output", "rowsum_o_do", "round_to_storage", "partial_attention",
+    "merge_two_halves",
 ]
 
 
@@ -117,6 +118,58 @@ def attention_bwd(q, k, v, do, causal: bool, scale: float):
             dq[b, h] = (dS @ k[b, h]) * scale
             dk[b, h] = (dS.T @ q[b, h]) * scale
     return dq, dk, dv
+
+
+def attention_bwd_from_output(q, k, v, o, do, L, causal: bool, scale: float):
+    """dQ, dK, dV by the backward pass with recomputation, handout Eq. 13-19.
+
+    Algorithm 2 of the handout takes the forward's output O and logsumexp L as
+    inputs next to Q, K, V and dO; D = rowsum(O * dO) is formed from that O.
+    With the exact O and L this equals ``attention_bwd`` (the D identity);
+    with O as the forward stores it (rounded to the storage dtype, handout
+    flash_forward (b): cast O to the input dtype before writing) it is the
+    exact result of the method's backward on the method's own stored output.
+      S = Q K^T * scale (Eq. 13),  P_ij = exp(S_ij - L_i) (Eq. 14),
+      dV = P^T dO (Eq. 15),  dP = dO V^T (Eq. 16),  dS_ij = P_ij (dP_ij - D_i) (Eq. 17),
+      dQ = dS K * scale (Eq. 18),  dK = dS^T Q * scale (Eq. 19).
+    """
+    q, k, v, o, do, L = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do), _f64(L)
+    B, H, S, d = q.shape
+    keep = causal_keep(S, S) if causal else None
+    D = rowsum_o_do(o, do)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    for b in range(B):
+        for h in range(H):
+            Sm = scores(q[b, h], k[b, h], scale)
+            P = np.exp(Sm - L[b, h][:, None])
+            if keep is not None:
+                P = np.where(keep, P, 0.0)
+            dv[b, h] = P.T @ do[b, h]
+            dP = do[b, h] @ v[b, h].T
+            dS = P * (dP - D[b, h][:, None])
+            dq[b, h] = (dS @ k[b, h]) * scale
+            dk[b, h] = (dS.T @ q[b, h]) * scale
+    return dq, dk, dv
+
+
+def round_to_storage(x, dtype: str) -> np.ndarray:
+    """Round values to the storage dtype and widen back to float64.
+
+    "fp32": round to the nearest float32.  "bf16": round to float32, then to
+    the nearest bfloat16 (8 significant bits, ties to even), the rounding a
+    store of an fp32 result to bfloat16 performs.  Finite inputs only.
+    """
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    if dtype == "fp32":
+        return x32.astype(np.float64)
+    if dtype != "bf16":
+        raise ValueError(dtype)
+    u = x32.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1                      # ties go to the even 16-bit result
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
 def rowsum_o_do(o, do) -> np.ndarray:

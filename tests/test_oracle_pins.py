@@ -259,3 +259,47 @@ def test_torch_sdpa_fp64_cross_check(causal):
     np.testing.assert_allclose(O, to.detach().numpy(), atol=1e-12)
     for a, t in ((dq, tq), (dk, tk), (dv, tv)):
         np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-12)
+
+
+# ---------------------------------------------------------------- recompute backward and storage rounding
+@pytest.mark.parametrize("causal", [False, True])
+def test_recompute_backward_equals_standard_with_exact_output(causal):
+    """Eq. 13-19 with the exact O and L give the same gradients as Eq. 7-11."""
+    S, d, sc = 11, 5, 0.45
+    q, k, v, do = (rnd(130 + s, 2, 2, S, d) for s in range(4))
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    g1 = oracle.attention_bwd(q, k, v, do, causal, sc)
+    g2 = oracle.attention_bwd_from_output(q, k, v, O, do, L, causal, sc)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(b, a, rtol=1e-11, atol=1e-13)
+
+
+def test_recompute_backward_uses_the_given_output():
+    """Perturbing O by e in one row moves D_i by e.dO_i, hence dQ_i by
+    -scale * (e.dO_i) * sum_j P_ij K_j and dK_j by -scale * (e.dO_i) P_ij Q_i."""
+    S, d, sc = 6, 3, 0.5
+    q, k, v, do = (rnd(140 + s, 1, 1, S, d) for s in range(4))
+    O, L = oracle.attention_fwd(q, k, v, False, sc)
+    e = rnd(144, d) * 1e-3
+    O2 = O.copy()
+    O2[0, 0, 2] += e
+    dq1, dk1, _ = oracle.attention_bwd_from_output(q, k, v, O, do, L, False, sc)
+    dq2, dk2, _ = oracle.attention_bwd_from_output(q, k, v, O2, do, L, False, sc)
+    dD = float(e @ do[0, 0, 2])
+    P = np.exp(sc * q[0, 0] @ k[0, 0].T - L[0, 0][:, None])
+    np.testing.assert_allclose(dq2[0, 0, 2] - dq1[0, 0, 2], -sc * dD * (P[2] @ k[0, 0]), atol=1e-14)
+    np.testing.assert_allclose(dk2[0, 0] - dk1[0, 0], -sc * dD * np.outer(P[2], q[0, 0, 2]), atol=1e-14)
+
+
+def test_round_to_bf16_closed_cases():
+    x = np.array([1.0, 1 + 2**-8, 1 + 3 * 2**-8, 1 + 2**-7, -3.0 - 2**-7, 2.0**-130, 65504.0, 0.0])
+    want = np.array([1.0, 1.0, 1 + 2**-6, 1 + 2**-7, -3.0, 2.0**-130, 65536.0, 0.0])
+    np.testing.assert_array_equal(oracle.round_to_storage(x, "bf16"), want)
+    np.testing.assert_array_equal(oracle.round_to_storage(np.array([1 + 2**-30]), "fp32"), [1.0])
+
+
+def test_round_to_bf16_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = rnd(150, 100000) * np.exp(rnd(151, 100000) * 5)
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_to_storage(x, "bf16"), ref)

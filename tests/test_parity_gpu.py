@@ -27,9 +27,13 @@ def built():
     fa.load_library()
 
 
-def run_gpu(q, k, v, do, causal, scale):
+def run_gpu(q, k, v, do, causal, scale, o_in=None, lse_in=None):
+    """fwd then bwd as a user calls them; with o_in/lse_in given, the backward
+    runs on those (host-made) tensors instead of the forward's outputs."""
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     o, lse = fa.fwd(qd, kd, vd, causal, scale)
+    if o_in is not None:
+        o, lse = o_in.to(DEV), lse_in.to(DEV)
     B, H, S, d = q.shape
     ws = torch.empty(fa.bwd_workspace_size(B, H, S, d, q.dtype), device=DEV, dtype=torch.uint8)
     dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, causal, scale, workspace=ws)
@@ -39,20 +43,30 @@ def run_gpu(q, k, v, do, causal, scale):
     return [t.cpu() for t in (o, lse, dq, dk, dv, D)]
 
 
-def check_heads(q, k, v, do, causal, scale, dtype, heads, res=None):
-    o, lse, dq, dk, dv, D = res if res is not None else run_gpu(q, k, v, do, causal, scale)
+def check_heads(q, k, v, do, causal, scale, dtype, heads):
+    """Compare sampled (b, h) slices with the oracle, twice:
+    (1) forward then backward on the forward's own outputs, as a user runs it;
+    (2) the backward alone on the oracle's stored O and L (fed from the host),
+        which also checks D = rowsum(O * dO) exactly on a known input."""
     tol = TOL[dtype]
-    for (b, h) in heads:
-        O, L, rdq, rdk, rdv = oracle_head(q, k, v, do, b, h, causal, scale)
+    refs = {(b, h): oracle_head(q, k, v, do, b, h, causal, scale, dtype) for (b, h) in heads}
+    o, lse, dq, dk, dv, _ = run_gpu(q, k, v, do, causal, scale)
+    B, H, S, d = q.shape
+    o_in = torch.zeros_like(q)
+    lse_in = torch.full((B, H, S), 1e4, dtype=torch.float32)   # P = 0 in unsampled heads
+    for (b, h), r in refs.items():
+        o_in[b, h] = torch.from_numpy(r["O_st"]).to(q.dtype)
+        lse_in[b, h] = torch.from_numpy(r["L_st"]).float()
+    _, _, dq2, dk2, dv2, D2 = run_gpu(q, k, v, do, causal, scale, o_in, lse_in)
+    for (b, h), r in refs.items():
         tag = f"[b={b},h={h},causal={causal}]"
-        assert_close("O" + tag, o[b, h], O, *tol["o"])
-        assert_close("L" + tag, lse[b, h], L, *tol["lse"])
-        assert_close("dQ" + tag, dq[b, h], rdq, *tol["grad"])
-        assert_close("dK" + tag, dk[b, h], rdk, *tol["grad"])
-        assert_close("dV" + tag, dv[b, h], rdv, *tol["grad"])
-        # D from the GPU's own stored O and the dO it was given.
-        Dref = oracle.rowsum_o_do(f64(o[b, h]), f64(do[b, h]))
-        assert_close("D" + tag, D[b, h], Dref, *tol["D"])
+        assert_close("O" + tag, o[b, h], r["O"], *tol["o"])
+        assert_close("L" + tag, lse[b, h], r["L"], *tol["lse"])
+        for name, g in (("dQ", dq), ("dK", dk), ("dV", dv)):
+            assert_close(name + tag, g[b, h], r[name.lower()], *tol["grad"])
+        for name, g in (("dQ", dq2), ("dK", dk2), ("dV", dv2)):
+            assert_close(name + " (bwd alone)" + tag, g[b, h], r[name.lower()], *tol["grad"])
+        assert_close("D" + tag, D2[b, h], r["D"], *tol["D"])
 
 
 def all_heads(B, H):
@@ -186,11 +200,11 @@ def test_autograd_function_matches_oracle():
     out = fa.attention(qd, kd, vd, causal=True)
     out.backward(do.to(DEV))
     for b, h in all_heads(1, 2):
-        O, L, rdq, rdk, rdv = oracle_head(q, k, v, do, b, h, True, 0.125)
-        assert_close("O", out[b, h].detach().cpu(), O, *TOL["bf16"]["o"])
-        assert_close("dQ", qd.grad[b, h].cpu(), rdq, *TOL["bf16"]["grad"])
-        assert_close("dK", kd.grad[b, h].cpu(), rdk, *TOL["bf16"]["grad"])
-        assert_close("dV", vd.grad[b, h].cpu(), rdv, *TOL["bf16"]["grad"])
+        r = oracle_head(q, k, v, do, b, h, True, 0.125, "bf16")
+        assert_close("O", out[b, h].detach().cpu(), r["O"], *TOL["bf16"]["o"])
+        assert_close("dQ", qd.grad[b, h].cpu(), r["dq"], *TOL["bf16"]["grad"])
+        assert_close("dK", kd.grad[b, h].cpu(), r["dk"], *TOL["bf16"]["grad"])
+        assert_close("dV", vd.grad[b, h].cpu(), r["dv"], *TOL["bf16"]["grad"])
 
 
 def test_device_errors_are_reported_not_raised_on_device():
