@@ -126,6 +126,8 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
 
 }  // namespace
 
+int fa::set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 int fa_profile_enable(int on) {

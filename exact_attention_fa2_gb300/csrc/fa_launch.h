@@ -50,6 +50,10 @@ cudaError_t launch_bwd_simt(const BwdArgs& a);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_dq_convert(const BwdArgs& a);
 
+// Record `msg` as the calling thread's last error (read by fa_get_last_error)
+// and return `code`.
+int set_last_error(int code, const char* msg);
+
 // bf16 tensor-core (tcgen05) kernels.
 cudaError_t launch_fwd_tc(const FwdArgs& a);
 cudaError_t launch_bwd_tc(const BwdArgs& a);

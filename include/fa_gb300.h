@@ -105,6 +105,37 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes,
            int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory.
+ * The pages describe no counterpart of this entry point; it exists for users
+ * of this library that cannot call cudaMalloc (or any allocating routine,
+ * PyTorch's caching allocator included) when they run the backward: code
+ * inside an allocator's own callbacks, runtimes that forbid allocation during
+ * a step, or plugins whose host owns all device memory.
+ *
+ * Same arguments and results as fa_bwd, minus the workspace: the workspace is
+ * a fixed array of FA_NOALLOC_SCRATCH_BYTES bytes compiled into the library
+ * (every GPU that loads the library holds it until the process exits).  The
+ * call allocates nothing.
+ *   - Problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
+ *     are rejected with FA_ERR_WORKSPACE and a message naming both sizes.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (D stays readable there; the dQ accumulator is zeroed by every
+ *     call).  Calls whose work overlaps on the GPU (different streams, or
+ *     host threads, without ordering between them) race on it and give wrong
+ *     results: order them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/* Size in bytes of the built-in scratch used by fa_bwd_noalloc. */
+size_t fa_bwd_noalloc_scratch_bytes(void);
+
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* fa_get_last_error(void);
 
