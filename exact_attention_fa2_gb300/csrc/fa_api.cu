@@ -174,7 +174,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     fa::FwdArgs a{q, k, v, o, lse, B, H, S, d, causal ? 1 : 0, scale, dtype,
                   static_cast<cudaStream_t>(stream), nullptr};
     if ((rc = status_ptr(&a.status))) return rc;
-    cudaError_t e = timed(PROF_FWD, a.stream, [&] { return fa::launch_fwd_simt(a); });
+    cudaError_t e = timed(PROF_FWD, a.stream, [&] {
+        return dtype == FA_BF16 ? fa::launch_fwd_tc(a) : fa::launch_fwd_simt(a);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return FA_OK;
 }

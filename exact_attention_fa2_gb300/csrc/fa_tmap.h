@@ -1,0 +1,16 @@
+// fa_tmap.h - TMA tensor maps over [B*H, S, d] bf16 tensors (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Encode a 3-D tiled tensor map over a contiguous [BH, S, d] bf16 array:
+// dimension 0 = d (innermost), 1 = S, 2 = BH; box = {box_w, box_rows, 1}.
+// The swizzle mode is chosen from the box's inner extent in bytes (32, 64 or
+// 128).  Out-of-range rows read as zero.  Returns cudaSuccess or an error.
+cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w,
+                              int box_rows);
+
+}  // namespace fa
