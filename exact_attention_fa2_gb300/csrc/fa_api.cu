@@ -213,7 +213,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if ((rc = status_ptr(&a.status))) return rc;
     cudaError_t e = timed(PROF_PRE, a.stream, [&] { return fa::launch_bwd_preprocess(a); });
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-    e = timed(PROF_BWD, a.stream, [&] { return fa::launch_bwd_simt(a); });
+    e = timed(PROF_BWD, a.stream, [&] {
+        return dtype == FA_BF16 ? fa::launch_bwd_tc(a) : fa::launch_bwd_simt(a);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     e = timed(PROF_CONV, a.stream, [&] { return fa::launch_dq_convert(a); });
     if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");

@@ -1,0 +1,477 @@
+// fa_bwd_tc.cu - bf16 FlashAttention-2 backward on the sm_103a tensor cores.
+//
+// "Stanford CS336 Assignment 2 (Systems)" handout, section 4: Eq. 13-19 with
+// the key-tile-outer loop of Algorithm 2.  One CTA owns a 128-key tile of one
+// (batch, head) and keeps its dK and dV accumulators in Tensor Memory while it
+// walks over the 128-row query tiles at or below the diagonal.  For each
+// query tile i (all products on tcgen05, fp32 accumulation):
+//   S^T  = K Q_i^T                 (key-major scores, Eq. 13)
+//   dP^T = V dO_i^T                (Eq. 16)
+//   P^T  = exp2(S^T c - L_i log2 e),  dS^T = P^T * (dP^T - D_i)   (Eq. 14, 17)
+//   dV  += P^T dO_i                (Eq. 15; P^T read from Tensor Memory)
+//   dK  += dS^T Q_i                (Eq. 19; dS^T from shared memory)
+//   dQ_i = dS K                    (Eq. 18; the same shared-memory dS^T tile
+//                                   read as an M-major operand)
+// dQ_i leaves Tensor Memory through a separate warpgroup that adds it into the
+// fp32 dQ accumulator with vector atomics (the stated dQ strategy); the scale
+// of Eq. 18 is applied when the accumulator is converted, that of Eq. 19 when
+// dK is written.
+//
+// Warp roles: warps 0-3 scores/softmax/dS (one thread per key row) and the
+// final dK/dV store, warps 4-7 the dQ read-out and atomics (one thread per
+// query row), warp 8 TMA (K, V once; Q_i, dO_i per tile, plus L and D), warp 9
+// Tensor Memory allocation and the single-thread MMA issuer.
+// Tensor Memory columns: dV [0,128), dK [128,256), S^T/P^T [256,384),
+// dP^T [384,512), which dQ_i reuses once dS^T has been formed.
+
+#include "fa_common.cuh"
+#include "fa_launch.h"
+#include "fa_tmap.h"
+#include "sm103_ptx.cuh"
+#include "fa_tc_common.cuh"
+
+#include <cstring>
+
+namespace fa {
+namespace {
+
+using namespace sm103;
+using namespace tc;
+
+constexpr int BK = 128;
+constexpr int BQ = 128;
+constexpr int NTHREADS = 320;
+constexpr int TMA_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
+constexpr int SMEM_BUDGET = 227 * 1024;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int TILE = 128 * D * 2;
+    static constexpr int DS_BYTES = BK * BQ * 2;
+    static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
+    static constexpr int FIXED = 2 * TILE + DS_BYTES;  // K, V, dS^T
+    static constexpr int STAGE = 2 * TILE + LD_BYTES;  // Q_i, dO_i, (L, D)_i
+    static constexpr int NS_RAW = (SMEM_BUDGET - FIXED - 256) / STAGE;
+    static constexpr int NS = NS_RAW > 3 ? 3 : NS_RAW;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = TILE;
+    static constexpr int DS_OFF = 2 * TILE;
+    static constexpr int Q_OFF = DS_OFF + DS_BYTES;
+    static constexpr int DO_OFF = Q_OFF + NS * TILE;
+    static constexpr int LD_OFF = DO_OFF + NS * TILE;
+    static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
+    // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, done, drain
+    static constexpr int NBARS = 7 + 2 * NS;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int BYTES = MISC_OFF + 16;
+    static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
+    static_assert(NS >= 2, "Q/dO ring needs two stages");
+    static_assert(BYTES <= SMEM_BUDGET, "shared memory budget");
+};
+
+struct BwdParams {
+    CUtensorMap tq[2];
+    CUtensorMap tk[2];
+    CUtensorMap tv[2];
+    CUtensorMap tdo[2];
+    const float* lse;
+    const float* Dvec;
+    float* dQacc;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    unsigned int* status;
+    int S;
+    int n_q;
+    int causal;
+    float c;          // |scale| * log2(e), at least 1e-30
+    float scale;      // signed scale applied to dK
+    uint32_t neg_a;   // 1 when scale < 0: S^T = -(K Q^T) so that exp uses |scale|
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// B operand of the products whose N dimension is the head dim: a [rows][d]
+// tile (TMA layout, 128 rows) read MN-major, k-step of 16 rows `ks`.
+template <int D>
+__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, bool a_in_tmem, uint32_t a_tm, uint64_t a_desc,
+                                           uint32_t b_tile, int ks, uint32_t a_mn, uint32_t acc) {
+    using C = Chunks<D>;
+    if constexpr (D == 128) {
+        const uint64_t bdesc = smem_desc(b_tile + ks * 16 * 128, 128 * 128, 1024, SW_128B);
+        if (a_in_tmem) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, 128, 0, 1), acc);
+        else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, 128, a_mn, 1), acc);
+    } else {
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+            const uint64_t bdesc = smem_desc(b_tile + C::tile_off(c, 128) + ks * 16 * C::row_bytes(c), 128 * 128,
+                                             8 * C::row_bytes(c), C::swz(c));
+            if (a_in_tmem) mma_ts(d_tmem + c * 64, a_tm, bdesc, idesc_bf16(128, C::width(c), 0, 1), acc);
+            else mma_ss(d_tmem + c * 64, a_desc, bdesc, idesc_bf16(128, C::width(c), a_mn, 1), acc);
+        }
+    }
+}
+
+// C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim contiguous).
+template <int D>
+__device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile, uint32_t idesc) {
+    using C = Chunks<D>;
+    int step = 0;
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c) {
+#pragma unroll
+        for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
+            const uint32_t off = C::tile_off(c, 128) + s * 32;
+            mma_ss(d_tmem, smem_desc(a_tile + off, 16, 8 * C::row_bytes(c), C::swz(c)),
+                   smem_desc(b_tile + off, 16, 8 * C::row_bytes(c), C::swz(c)), idesc, step > 0 ? 1u : 0u);
+        }
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+    using C = Chunks<D>;
+    using G = BwdCfg<D>;
+    constexpr int NS = G::NS;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (smem + G::BYTES > smem_raw + G::DYN_SMEM) {
+        // The dynamic shared window is not 1024-byte aligned and has no room to
+        // align it: report and leave before touching any barrier or TMEM.
+        if (threadIdx.x == 0) set_status(p.status, FA_DEV_STATUS_BOUNDS);
+        return;
+    }
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + G::BAR_OFF;
+    const uint32_t kv_full = bar0;
+    auto q_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto q_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
+    const uint32_t s_full = bar0 + 8u * (1 + 2 * NS);
+    const uint32_t p_full = s_full + 8;
+    const uint32_t dq_full = s_full + 16;
+    const uint32_t dq_empty = s_full + 24;
+    const uint32_t done = s_full + 32;
+    const uint32_t drain = s_full + 40;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
+    volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int j = blockIdx.x;                 // key tile; early tiles see the most query tiles
+    const int bh = blockIdx.y;
+    const int S = p.S;
+    const int k0 = j * BK;
+    const int i0 = p.causal ? j : 0;          // query tiles above the diagonal are fully masked
+    const int n_it = p.n_q - i0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(q_full(s), 33);        // TMA expect-tx arrival + 32 lanes that stage (L, D)
+            mbar_init(q_empty(s), 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, BK);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, BQ);
+        mbar_init(done, 1);
+        mbar_init(drain, 1);
+        *abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == TMA_WARP) {
+        // ------------------------------------------------------------ producer
+        int issued = 0;
+        if (lane == 0) {
+            for (int i = 0; i < 2; ++i) {
+                prefetch_tmap(&p.tq[i]);
+                prefetch_tmap(&p.tk[i]);
+                prefetch_tmap(&p.tv[i]);
+                prefetch_tmap(&p.tdo[i]);
+            }
+            mbar_arrive_expect_tx(kv_full, 2 * G::TILE);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+                tma_load_3d(sb + G::K_OFF + C::tile_off(c, BK), &p.tk[C::map_index(c)], c * 64, k0, bh, kv_full);
+                tma_load_3d(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], c * 64, k0, bh, kv_full);
+            }
+        }
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1;
+            const int q0 = (i0 + it) * BQ;
+            if (!warp_wait(q_empty(s), ph ^ 1, abort, p.status)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full(s), 2 * G::TILE);
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c) {
+                    tma_load_3d(sb + G::Q_OFF + s * G::TILE + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64,
+                                q0, bh, q_full(s));
+                    tma_load_3d(sb + G::DO_OFF + s * G::TILE + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64,
+                                q0, bh, q_full(s));
+                }
+            }
+            // (L * log2 e, D) for the 128 query rows; rows past S get (+inf, 0) so P = 0.
+            const size_t rb = (size_t)bh * S;
+#pragma unroll
+            for (int e = 0; e < BQ / 32; ++e) {
+                const int qr = e * 32 + lane;
+                const int q = q0 + qr;
+                const float l2 = q < S ? p.lse[rb + q] * FA_LOG2E : INFINITY;
+                const float dd = q < S ? p.Dvec[rb + q] : 0.f;
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(sb + G::LD_OFF + s * G::LD_BYTES + qr * 8),
+                             "f"(l2), "f"(dd) : "memory");
+            }
+            mbar_arrive(q_full(s));
+            issued = it + 1;
+        }
+        if (*abort && lane == 0) {
+            volatile int no_abort = 0;
+            mbar_wait(kv_full, 0, &no_abort, p.status, WAIT_LIMIT_NS);
+            for (int it = max(0, issued - NS); it < issued; ++it)
+                mbar_wait(q_full(it % NS), (it / NS) & 1, &no_abort, p.status, WAIT_LIMIT_NS);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0) | (p.neg_a << 13);
+        const uint32_t idesc_dp = idesc_bf16(128, 128, 0, 0);
+        bool ok = warp_wait(kv_full, 0, abort, p.status);
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1;
+            const uint32_t qt = sb + G::Q_OFF + s * G::TILE;
+            const uint32_t dot = sb + G::DO_OFF + s * G::TILE;
+            if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
+            tc_fence_after();
+            if (lane == 0) mma_k_is_d<D>(tmem + TM_S, sb + G::K_OFF, qt, idesc_s);       // S^T = K Q^T
+            if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+            tc_fence_after();
+            if (lane == 0) {
+                mma_k_is_d<D>(tmem + TM_DP, sb + G::V_OFF, dot, idesc_dp);               // dP^T = V dO^T
+                mma_commit(s_full);
+            }
+            if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks) {                                     // dV += P^T dO
+                    mma_n_is_d<D>(tmem + TM_DV, true, tmem + TM_S + ks * 8, 0, dot, ks, 0,
+                                  (it > 0 || ks > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks) {                                     // dK += dS^T Q
+                    const uint64_t adesc = smem_desc(sb + G::DS_OFF + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, SW_128B);
+                    mma_n_is_d<D>(tmem + TM_DK, false, 0, adesc, qt, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int ks = 0; ks < BK / 16; ++ks) {                                     // dQ_i = dS K
+                    const uint64_t adesc = smem_desc(sb + G::DS_OFF + ks * 2048, 16384, 1024, SW_128B);
+                    mma_n_is_d<D>(tmem + TM_DP, false, 0, adesc, sb + G::K_OFF, ks, 1, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(dq_full);
+                mma_commit(q_empty(s));
+            }
+            __syncwarp();
+        }
+        if (ok && lane == 0) mma_commit(done);
+        if (*abort) {
+            if (lane == 0) {
+                volatile int no_abort = 0;
+                mma_commit(drain);
+                mbar_wait(drain, 0, &no_abort, p.status, WAIT_LIMIT_NS);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ P^T, dS^T and the dK/dV store
+        const int jr = warp * 32 + lane;               // key row inside the tile
+        const int key = k0 + jr;
+        const bool key_ok = key < S;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + TM_S;
+        const uint32_t tP = tmem + lane_off + TM_DP;
+        const float c = p.c;
+        const uint32_t ds_row = sb + G::DS_OFF + jr * 128;
+        const uint32_t swz = (uint32_t)(jr & 7);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1;
+            const bool diag = p.causal && (i0 + it) == j;
+            if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
+            if (!(ok = warp_wait(s_full, it & 1, abort, p.status))) break;
+            tc_fence_after();
+            const uint32_t ldb = sb + G::LD_OFF + s * G::LD_BYTES;
+#pragma unroll
+            for (int qq = 0; qq < BQ / 32; ++qq) {
+                uint32_t rs[32], rp[32];
+                tmem_ld32(tS + 32 * qq, rs);
+                tmem_ld32(tP + 32 * qq, rp);
+                tmem_wait_ld();
+                reg_fence<32>(rs);
+                reg_fence<32>(rp);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int q = 32 * qq + 2 * e;                          // query column inside the tile
+                    const float4 ld = ld_shared_f4(ldb + q * 8);           // (L2, D) of q and q+1
+                    float p0 = ex2(fmaf(__uint_as_float(rs[2 * e]), c, -ld.x));
+                    float p1 = ex2(fmaf(__uint_as_float(rs[2 * e + 1]), c, -ld.z));
+                    if (!key_ok || (diag && q < jr)) p0 = 0.f;
+                    if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
+                    const float d0 = p0 * (__uint_as_float(rp[2 * e]) - ld.y);
+                    const float d1 = p1 * (__uint_as_float(rp[2 * e + 1]) - ld.w);
+                    pk[e] = pack_bf16(p0, p1);
+                    dk[e] = pack_bf16(d0, d1);
+                }
+                tmem_st16(tS + 16 * qq, pk);
+                // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
+                // 128-byte-swizzled [key][query] tile (two 64-query chunks).
+                const uint32_t chunk = ds_row + (uint32_t)(qq >> 1) * 16384;
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const uint32_t u = (uint32_t)((qq & 1) * 4 + u4);
+                    st_shared_v4(chunk + ((u ^ swz) << 4), dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        // dK, dV rows of this key tile.
+        if (ok && warp_wait(done, 0, abort, p.status)) {
+            tc_fence_after();
+            const size_t row = (size_t)bh * S + key;
+#pragma unroll
+            for (int u = 0; u < D / 16; ++u) {
+                uint32_t a[16], b[16];
+                tmem_ld16(tmem + lane_off + TM_DV + 16 * u, a);
+                tmem_ld16(tmem + lane_off + TM_DK + 16 * u, b);
+                tmem_wait_ld();
+                reg_fence<16>(a);
+                reg_fence<16>(b);
+                uint32_t va[8], vb[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    va[e] = pack_bf16(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                    vb[e] = pack_bf16(__uint_as_float(b[2 * e]) * p.scale, __uint_as_float(b[2 * e + 1]) * p.scale);
+                }
+                if (key_ok) {
+                    uint4* dvp = reinterpret_cast<uint4*>(p.dv + row * D + 16 * u);
+                    uint4* dkp = reinterpret_cast<uint4*>(p.dk + row * D + 16 * u);
+                    dvp[0] = make_uint4(va[0], va[1], va[2], va[3]);
+                    dvp[1] = make_uint4(va[4], va[5], va[6], va[7]);
+                    dkp[0] = make_uint4(vb[0], vb[1], vb[2], vb[3]);
+                    dkp[1] = make_uint4(vb[4], vb[5], vb[6], vb[7]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ dQ_i read-out and atomics
+        const int wq = warp & 3;
+        const int qr = wq * 32 + lane;                 // query row inside the tile
+        const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM_DP;
+        for (int it = 0; it < n_it; ++it) {
+            if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
+            tc_fence_after();
+            const int q = (i0 + it) * BQ + qr;
+            float* dst = p.dQacc + ((size_t)bh * S + q) * D;
+            uint32_t r[D];
+#pragma unroll
+            for (int u = 0; u < D / 16; ++u) tmem_ld16(tQ + 16 * u, r + 16 * u);
+            tmem_wait_ld();
+            reg_fence<D>(r);
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+            if (q < S) {
+#pragma unroll
+                for (int u = 0; u < D / 4; ++u)
+                    red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                               __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int D>
+cudaError_t bwd_tc_launch(const BwdArgs& a) {
+    using C = Chunks<D>;
+    using G = BwdCfg<D>;
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    const int BH = a.B * a.H;
+    const void* src[4] = {a.q, a.k, a.v, a.dO};
+    CUtensorMap* maps[4] = {p.tq, p.tk, p.tv, p.tdo};
+    for (int i = 0; i < 4; ++i) {
+        cudaError_t e;
+        if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, 128)) != cudaSuccess) return e;
+        if (C::REM > 0 && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess) return e;
+    }
+    p.lse = a.lse;
+    p.Dvec = a.Dvec;
+    p.dQacc = a.dQacc;
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    p.status = a.status;
+    p.S = a.S;
+    p.n_q = (a.S + BQ - 1) / BQ;
+    p.causal = a.causal;
+    const float c = fabsf(a.scale) * FA_LOG2E;
+    p.c = c < 1e-30f ? 1e-30f : c;
+    p.scale = a.scale;
+    p.neg_a = a.scale < 0.f ? 1u : 0u;
+    auto kern = bwd_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.S + BK - 1) / BK, BH);
+    kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs& a) {
+    switch (a.d) {
+        case 16: return bwd_tc_launch<16>(a);
+        case 32: return bwd_tc_launch<32>(a);
+        case 64: return bwd_tc_launch<64>(a);
+        case 80: return bwd_tc_launch<80>(a);
+        case 96: return bwd_tc_launch<96>(a);
+        case 128: return bwd_tc_launch<128>(a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa
