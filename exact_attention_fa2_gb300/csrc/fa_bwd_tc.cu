@@ -107,37 +107,41 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 
 // B operand of the products whose N dimension is the head dim: a [rows][d]
 // tile (TMA layout, 128 rows) read MN-major, k-step of 16 rows `ks`.
-template <int D>
-__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, bool a_in_tmem, uint32_t a_tm, uint64_t a_desc,
-                                           uint32_t b_tile, int ks, uint32_t a_mn, uint32_t acc) {
+// `b_lo` is the low descriptor word of the tile (LBO = the 64-column chunk
+// stride); the A operand is either Tensor Memory (`a_tm`) or shared memory
+// (`a_desc`).
+template <int D, bool A_TMEM>
+__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint64_t a_desc, uint32_t b_lo, int ks,
+                                           uint32_t a_mn, uint32_t acc) {
     using C = Chunks<D>;
     if constexpr (D == 128) {
-        const uint64_t bdesc = smem_desc(b_tile + ks * 16 * 128, 128 * 128, 1024, SW_128B);
-        if (a_in_tmem) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, 128, 0, 1), acc);
+        const uint64_t bdesc = desc_make(b_lo + ks * 128, desc_hi(1024, SW_128B));
+        if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, 128, 0, 1), acc);
         else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, 128, a_mn, 1), acc);
     } else {
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-            const uint64_t bdesc = smem_desc(b_tile + C::tile_off(c, 128) + ks * 16 * C::row_bytes(c), 128 * 128,
-                                             8 * C::row_bytes(c), C::swz(c));
-            if (a_in_tmem) mma_ts(d_tmem + c * 64, a_tm, bdesc, idesc_bf16(128, C::width(c), 0, 1), acc);
+            const uint32_t off = (C::tile_off(c, 128) + ks * 16 * C::row_bytes(c)) >> 4;
+            const uint64_t bdesc = desc_make(b_lo + off, desc_hi(8 * C::row_bytes(c), C::swz(c)));
+            if constexpr (A_TMEM) mma_ts(d_tmem + c * 64, a_tm, bdesc, idesc_bf16(128, C::width(c), 0, 1), acc);
             else mma_ss(d_tmem + c * 64, a_desc, bdesc, idesc_bf16(128, C::width(c), a_mn, 1), acc);
         }
     }
 }
 
-// C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim contiguous).
+// C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim
+// contiguous); a_lo / b_lo are the tiles' low descriptor words (LBO 16).
 template <int D>
-__device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile, uint32_t idesc) {
+__device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
     using C = Chunks<D>;
     int step = 0;
 #pragma unroll
     for (int c = 0; c < C::NCH; ++c) {
 #pragma unroll
         for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
-            const uint32_t off = C::tile_off(c, 128) + s * 32;
-            mma_ss(d_tmem, smem_desc(a_tile + off, 16, 8 * C::row_bytes(c), C::swz(c)),
-                   smem_desc(b_tile + off, 16, 8 * C::row_bytes(c), C::swz(c)), idesc, step > 0 ? 1u : 0u);
+            const uint32_t off = (C::tile_off(c, 128) + s * 32) >> 4;
+            const uint32_t hi = desc_hi(8 * C::row_bytes(c), C::swz(c));
+            mma_ss(d_tmem, desc_make(a_lo + off, hi), desc_make(b_lo + off, hi), idesc, step > 0 ? 1u : 0u);
         }
     }
 }
@@ -261,38 +265,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0) | (p.neg_a << 13);
         const uint32_t idesc_dp = idesc_bf16(128, 128, 0, 0);
+        // Low descriptor words: K-major operands use LBO 16, the MN-major
+        // [rows][d] tiles use the 64-column chunk stride as LBO.
+        const uint32_t k_lo = desc_lo(sb + G::K_OFF, 16), v_lo = desc_lo(sb + G::V_OFF, 16);
+        const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, 128 * 128);
+        const uint32_t q_lo0 = desc_lo(sb + G::Q_OFF, 16), do_lo0 = desc_lo(sb + G::DO_OFF, 16);
+        const uint32_t q_mn_lo0 = desc_lo(sb + G::Q_OFF, 128 * 128), do_mn_lo0 = desc_lo(sb + G::DO_OFF, 128 * 128);
+        const uint32_t ds_k_lo = desc_lo(sb + G::DS_OFF, 16);          // dS^T as K-major A (dK)
+        const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);       // dS as M-major A (dQ)
+        const uint32_t ds_hi = desc_hi(1024, SW_128B);
         bool ok = warp_wait(kv_full, 0, abort, p.status);
         for (int it = 0; it < n_it && ok; ++it) {
             const int s = it % NS;
             const uint32_t ph = (it / NS) & 1;
-            const uint32_t qt = sb + G::Q_OFF + s * G::TILE;
-            const uint32_t dot = sb + G::DO_OFF + s * G::TILE;
+            const uint32_t so = (uint32_t)s * (G::TILE >> 4);
             if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
             tc_fence_after();
-            if (lane == 0) mma_k_is_d<D>(tmem + TM_S, sb + G::K_OFF, qt, idesc_s);       // S^T = K Q^T
+            if (lane == 0) mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);         // S^T = K Q^T
             if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) {
-                mma_k_is_d<D>(tmem + TM_DP, sb + G::V_OFF, dot, idesc_dp);               // dP^T = V dO^T
+                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
                 mma_commit(s_full);
             }
             if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) {
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks) {                                     // dV += P^T dO
-                    mma_n_is_d<D>(tmem + TM_DV, true, tmem + TM_S + ks * 8, 0, dot, ks, 0,
-                                  (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < BQ / 16; ++ks)                                        // dV += P^T dO
+                    mma_n_is_d<D, true>(tmem + TM_DV, tmem + TM_S + ks * 8, 0, do_mn_lo0 + so, ks, 0,
+                                        (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
+                    const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
+                    mma_n_is_d<D, false>(tmem + TM_DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                 }
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks) {                                     // dK += dS^T Q
-                    const uint64_t adesc = smem_desc(sb + G::DS_OFF + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024, SW_128B);
-                    mma_n_is_d<D>(tmem + TM_DK, false, 0, adesc, qt, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks) {                                     // dQ_i = dS K
-                    const uint64_t adesc = smem_desc(sb + G::DS_OFF + ks * 2048, 16384, 1024, SW_128B);
-                    mma_n_is_d<D>(tmem + TM_DP, false, 0, adesc, sb + G::K_OFF, ks, 1, ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < BK / 16; ++ks) {                                      // dQ_i = dS K
+                    const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
+                    mma_n_is_d<D, false>(tmem + TM_DP, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(dq_full);
                 mma_commit(q_empty(s));

@@ -4,25 +4,26 @@
 // Assignment 2 (Systems)" handout, section 4: Eq. 4-6, Eq. 12, Algorithm 1)
 // with tcgen05.mma into Tensor Memory.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and streams the
-// 128-key K/V tiles they need through a TMA/mbarrier ring.  Warp roles:
-//   warps 0-3  softmax for query tile 0 (one thread per query row),
-//   warps 4-7  softmax for query tile 1,
-//   warp  8    TMA producer (Q tiles once, then the K and V rings),
+// One CTA owns one 128-row query tile of one (batch, head) and streams the
+// 128-key K/V tiles it needs through a TMA/mbarrier ring.  Warp roles:
+//   warps 0-3  softmax on score columns 0-63 (one query row per thread),
+//   warps 4-7  softmax on score columns 64-127 (same rows),
+//   warp  8    TMA producer (Q once, then the K and V rings),
 //   warp  9    Tensor Memory allocation and the single-thread MMA issuer.
-// Tensor Memory (512 columns): S_t in columns [128t, 128t+128) for the two
-// tiles, O_t in [256+128t, 256+128t+d).  P_t (bf16) overwrites the first 64
-// columns of S_t and is read from there by the PV product.  While one tile's
-// softmax runs, the tensor cores work on the other tile (ping-pong).
+// Tensor Memory: two score buffers S_0, S_1 (columns [0,128) and [128,256))
+// and the output accumulator O (columns [256, 256+d)).  The MMA issuer
+// computes S_{j+1} = Q K_{j+1}^T into the free buffer while the softmax works
+// on S_j, so the tensor cores and the softmax warps run concurrently.  P_j
+// (bf16) overwrites the first 64 columns of its score buffer and the PV
+// product reads it from there.
 //
 // Online softmax (Algorithm 1 lines 10-13) in base 2: scores are scaled by
-// c = |scale| * log2(e).  A warp rescales its rows of O in Tensor Memory only
-// when some row's running max grew; rows whose max did not grow multiply by 1.
+// c = |scale| * log2(e); the two halves of a row exchange their maxima through
+// shared memory; a warp rescales its rows of O only when some row's max grew.
 // The running max is always the exact max so far, which keeps the dominant
 // probability of a sharp row at exactly 1.0 before the bf16 rounding of P
-// (letting the max lag by a few binades would double the bf16 error of O for
-// sharp softmax rows).
-// Fully masked causal tiles are never loaded or multiplied.
+// (letting the max lag by a few binades doubles the bf16 error of O for sharp
+// softmax rows).  Fully masked causal tiles are never loaded or multiplied.
 
 #include "fa_common.cuh"
 #include "fa_launch.h"
@@ -44,20 +45,21 @@ constexpr int NTHREADS = 320;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr float RESCALE_THRESHOLD = 0.0f;
+constexpr uint32_t TM_O = 256;
 constexpr int SMEM_FLOOR = 120 * 1024;   // keeps one CTA per SM (it owns all of TMEM)
 
 template <int D>
 struct FwdCfg {
     static constexpr int TILE = BM * D * 2;
-    static constexpr int NS_RAW = (225 * 1024 - 2 * TILE) / (2 * TILE);
+    static constexpr int NS_RAW = (222 * 1024 - TILE) / (2 * TILE);
     static constexpr int NS = NS_RAW > 4 ? 4 : NS_RAW;
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + 2 * TILE;
+    static constexpr int K_OFF = Q_OFF + TILE;
     static constexpr int V_OFF = K_OFF + NS * TILE;
-    static constexpr int BAR_OFF = V_OFF + NS * TILE;
-    // q_full[2], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_full[2], drain
-    static constexpr int NBARS = 2 + 4 * NS + 7;
+    static constexpr int X_OFF = V_OFF + NS * TILE;     // (value, tag) slots: max [2 parity][2 half][128], l [2 half][128]
+    static constexpr int BAR_OFF = X_OFF + 6 * BM * 8;
+    // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full, o_done, drain
+    static constexpr int NBARS = 1 + 4 * NS + 5;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) > SMEM_FLOOR ? (BYTES + 1024) : SMEM_FLOOR;
@@ -73,12 +75,38 @@ struct FwdParams {
     float* lse;
     unsigned int* status;
     int S;
-    int n_pairs;
+    int n_qt;
     int n_kv;
     int causal;
     float c;          // |scale| * log2(e), at least 1e-30
     uint32_t neg_a;   // 1 when scale < 0: the S product negates Q
 };
+
+// Exchange one float with the partner thread that owns the other column half
+// of the same query row: publish (value, tag) with one 64-bit store, then poll
+// the partner's slot until it carries the same tag.  The poll is bounded: on
+// timeout (or when another role of the CTA gave up) it reports through the
+// status word / abort flag and returns the thread's own value.
+__device__ __forceinline__ float exchange_with_partner(uint32_t mine, uint32_t theirs, float val, int tag,
+                                                       volatile int* abort, unsigned int* status, bool& ok) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(mine), "f"(val), "f"(__int_as_float(tag)) : "memory");
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        float pv, pt;
+        asm volatile("ld.volatile.shared.v2.f32 {%0, %1}, [%2];" : "=f"(pv), "=f"(pt) : "r"(theirs) : "memory");
+        if (__float_as_int(pt) == tag) return pv;
+        if ((n & 255) == 255) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            if (*abort || now - t0 > WAIT_LIMIT_NS) {
+                if (!*abort) set_status(status, FA_DEV_STATUS_TIMEOUT);
+                *abort = 1;
+                ok = false;
+                return val;
+            }
+        }
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
@@ -90,45 +118,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
     const uint32_t bar0 = sb + G::BAR_OFF;
-    auto q_full = [&](int t) { return bar0 + 8u * t; };
-    auto k_full = [&](int s) { return bar0 + 8u * (2 + s); };
-    auto k_empty = [&](int s) { return bar0 + 8u * (2 + NS + s); };
-    auto v_full = [&](int s) { return bar0 + 8u * (2 + 2 * NS + s); };
-    auto v_empty = [&](int s) { return bar0 + 8u * (2 + 3 * NS + s); };
-    auto s_full = [&](int t) { return bar0 + 8u * (2 + 4 * NS + t); };
-    auto p_full = [&](int t) { return bar0 + 8u * (4 + 4 * NS + t); };
-    auto o_full = [&](int t) { return bar0 + 8u * (6 + 4 * NS + t); };
-    const uint32_t drain = bar0 + 8u * (8 + 4 * NS);
+    const uint32_t q_full = bar0;
+    auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
+    auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * NS + s); };
+    auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * NS + s); };
+    auto s_full = [&](int b) { return bar0 + 8u * (1 + 4 * NS + b); };
+    const uint32_t p_full = bar0 + 8u * (3 + 4 * NS);
+    const uint32_t o_done = bar0 + 8u * (4 + 4 * NS);
+    const uint32_t drain = bar0 + 8u * (5 + 4 * NS);
+    const uint32_t xmax = sb + G::X_OFF;                               // float2 slots [2][2][128]
+    const uint32_t xl = xmax + 4 * BM * 8;                              // float2 slots [2][128]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int pair = p.causal ? (p.n_pairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int qt = p.causal ? (p.n_qt - 1 - (int)blockIdx.x) : (int)blockIdx.x;   // long rows first
     const int bh = blockIdx.y;
     const int S = p.S;
-
-    // Query tile t covers rows [q0(t), q0(t)+128) and needs key tiles 0..jmax(t).
-    auto q0 = [&](int t) { return pair * 2 * BM + t * BM; };
-    auto active = [&](int t) { return q0(t) < S; };
-    auto jmax = [&](int t) { return p.causal ? min(2 * pair + t, p.n_kv - 1) : p.n_kv - 1; };
-    const int n_iter = (active(1) ? max(jmax(0), jmax(1)) : jmax(0)) + 1;
+    const int q0 = qt * BM;
+    const int jmax = p.causal ? min(qt, p.n_kv - 1) : p.n_kv - 1;   // key tiles 0..jmax
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(q_full(t), 1);
-            mbar_init(s_full(t), 1);
-            mbar_init(p_full(t), BM);
-            mbar_init(o_full(t), 1);
-        }
+        mbar_init(q_full, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
+        mbar_init(s_full(0), 1);
+        mbar_init(s_full(1), 1);
+        mbar_init(p_full, 2 * BM);
+        mbar_init(o_done, 1);
         mbar_init(drain, 1);
         *abort = 0;
+    }
+    for (int i = threadIdx.x; i < 6 * BM; i += NTHREADS)            // no slot carries a valid tag yet
+        reinterpret_cast<int2*>(smem + G::X_OFF)[i] = make_int2(0, -1);
+    if (threadIdx.x == 0) {
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -150,15 +179,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
                 prefetch_tmap(&p.tk[i]);
                 prefetch_tmap(&p.tv[i]);
             }
-            for (int t = 0; t < 2; ++t) {
-                if (!active(t)) continue;
-                mbar_arrive_expect_tx(q_full(t), G::TILE);
+            mbar_arrive_expect_tx(q_full, G::TILE);
 #pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sb + G::Q_OFF + t * G::TILE + C::tile_off(c, BM), &p.tq[C::map_index(c)],
-                                c * 64, q0(t), bh, q_full(t));
-            }
-            for (int j = 0; j < n_iter; ++j) {
+            for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sb + G::Q_OFF + C::tile_off(c, BM), &p.tq[C::map_index(c)], c * 64, q0, bh, q_full);
+            for (int j = 0; j <= jmax; ++j) {
                 const int st = j % NS;
                 const uint32_t ph = (j / NS) & 1;
                 if (!mbar_wait(k_empty(st), ph ^ 1, abort, p.status, WAIT_LIMIT_NS)) break;
@@ -179,6 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             if (*abort) {
                 // Let the copies already in flight land before the CTA exits.
                 volatile int no_abort = 0;
+                mbar_wait(q_full, 0, &no_abort, p.status, WAIT_LIMIT_NS);
                 for (int j = max(0, issued_k - NS); j < issued_k; ++j)
                     mbar_wait(k_full(j % NS), (j / NS) & 1, &no_abort, p.status, WAIT_LIMIT_NS);
                 for (int j = max(0, issued_v - NS); j < issued_v; ++j)
@@ -189,76 +215,70 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc_s = idesc_bf16(BM, BN, 0, 0) | (p.neg_a << 13);
-        bool ok = true;
-        for (int t = 0; t < 2 && ok; ++t)
-            if (active(t)) ok = warp_wait(q_full(t), 0, abort, p.status);
-        for (int j = 0; j <= n_iter && ok; ++j) {
+        // Low descriptor words of the operand buffers; k-steps add constants.
+        const uint32_t q_lo = desc_lo(sb + G::Q_OFF, 16);
+        const uint32_t k_lo0 = desc_lo(sb + G::K_OFF, 16);
+        const uint32_t v_lo0 = desc_lo(sb + G::V_OFF, BN * 128);
+        // S_j = Q K_j^T into score buffer j % 2.
+        auto issue_s = [&](int j) {
             const int st = j % NS;
-            const uint32_t ph = (j / NS) & 1;
-            const int sp = (j + NS - 1) % NS;
-            const uint32_t pph = ((j - 1) / NS) & 1;
-            if (j < n_iter && !(ok = warp_wait(k_full(st), ph, abort, p.status))) break;
-            bool v_ready = false;
+            const uint32_t d_s = tmem + (uint32_t)(j & 1) * 128;
+            const uint32_t klo = k_lo0 + (uint32_t)st * (G::TILE >> 4);
+            int step = 0;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (!active(t)) continue;
-                if (j >= 1 && j - 1 <= jmax(t)) {
-                    if (!v_ready) {
-                        if (!(ok = warp_wait(v_full(sp), pph, abort, p.status))) break;
-                        v_ready = true;
-                    }
-                    if (!(ok = warp_wait(p_full(t), (j - 1) & 1, abort, p.status))) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        // O_t += P_t V_{j-1}: A = P from TMEM, B = V (MN-major, keys along K).
-                        const uint32_t d_o = tmem + 256 + t * 128;
-                        const uint32_t vbase = sb + G::V_OFF + sp * G::TILE;
+            for (int c = 0; c < C::NCH; ++c) {
 #pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks) {
-                            const uint32_t a_tm = tmem + t * 128 + ks * 8;
-                            const uint32_t acc = (j - 1 > 0 || ks > 0) ? 1u : 0u;
-                            if constexpr (D == 128) {
-                                const uint64_t bdesc = smem_desc(vbase + ks * 16 * 128, BN * 128, 1024, SW_128B);
-                                mma_ts(d_o, a_tm, bdesc, idesc_bf16(BM, 128, 0, 1), acc);
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < C::NCH; ++c) {
-                                    const uint64_t bdesc = smem_desc(
-                                        vbase + C::tile_off(c, BN) + ks * 16 * C::row_bytes(c), BN * 128,
-                                        8 * C::row_bytes(c), C::swz(c));
-                                    mma_ts(d_o + c * 64, a_tm, bdesc, idesc_bf16(BM, C::width(c), 0, 1), acc);
-                                }
-                            }
-                        }
-                        if (j - 1 == jmax(t)) mma_commit(o_full(t));
-                    }
+                for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
+                    const uint32_t off = (C::tile_off(c, BM) + s * 32) >> 4;
+                    const uint32_t hi = desc_hi(8 * C::row_bytes(c), C::swz(c));
+                    mma_ss(d_s, desc_make(q_lo + off, hi), desc_make(klo + off, hi), idesc_s, step > 0 ? 1u : 0u);
                 }
-                if (j < n_iter && j <= jmax(t)) {
-                    if (lane == 0) {
-                        // S_t = Q_t K_j^T: both operands K-major (head dim contiguous).
-                        const uint32_t d_s = tmem + t * 128;
-                        const uint32_t qbase = sb + G::Q_OFF + t * G::TILE;
-                        const uint32_t kbase = sb + G::K_OFF + st * G::TILE;
-                        int step = 0;
+            }
+            mma_commit(s_full(j & 1));
+            mma_commit(k_empty(st));
+        };
+        // O += P_j V_j: A = P_j from Tensor Memory, B = V_j (MN-major, keys along K).
+        auto issue_pv = [&](int j) {
+            const int st = j % NS;
+            const uint32_t vlo = v_lo0 + (uint32_t)st * (G::TILE >> 4);
 #pragma unroll
-                        for (int c = 0; c < C::NCH; ++c) {
+            for (int ks = 0; ks < BN / 16; ++ks) {
+                const uint32_t a_tm = tmem + (uint32_t)(j & 1) * 128 + ks * 8;
+                const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+                if constexpr (D == 128) {
+                    mma_ts(tmem + TM_O, a_tm, desc_make(vlo + ks * 128, desc_hi(1024, SW_128B)),
+                           idesc_bf16(BM, 128, 0, 1), acc);
+                } else {
 #pragma unroll
-                            for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
-                                const uint32_t off = C::tile_off(c, BM) + s * 32;
-                                const uint64_t adesc = smem_desc(qbase + off, 16, 8 * C::row_bytes(c), C::swz(c));
-                                const uint64_t bdesc = smem_desc(kbase + off, 16, 8 * C::row_bytes(c), C::swz(c));
-                                mma_ss(d_s, adesc, bdesc, idesc_s, step > 0 ? 1u : 0u);
-                            }
-                        }
-                        mma_commit(s_full(t));
+                    for (int c = 0; c < C::NCH; ++c) {
+                        const uint32_t off = (C::tile_off(c, BN) + ks * 16 * C::row_bytes(c)) >> 4;
+                        mma_ts(tmem + TM_O + c * 64, a_tm, desc_make(vlo + off, desc_hi(8 * C::row_bytes(c), C::swz(c))),
+                               idesc_bf16(BM, C::width(c), 0, 1), acc);
                     }
                 }
             }
-            if (!ok) break;
-            if (lane == 0) {
-                if (j < n_iter) mma_commit(k_empty(st));
-                if (j >= 1) mma_commit(v_empty(sp));
+            mma_commit(o_done);
+            mma_commit(v_empty(st));
+        };
+        bool ok = warp_wait(q_full, 0, abort, p.status);
+        if (ok) ok = warp_wait(k_full(0), 0, abort, p.status);
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) issue_s(0);
+            __syncwarp();
+        }
+        for (int j = 0; j <= jmax && ok; ++j) {
+            if (j + 1 <= jmax) {
+                const int st = (j + 1) % NS;
+                if (!(ok = warp_wait(k_full(st), ((j + 1) / NS) & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) issue_s(j + 1);
+                __syncwarp();
             }
+            if (!(ok = warp_wait(v_full(j % NS), (j / NS) & 1, abort, p.status))) break;
+            if (!(ok = warp_wait(p_full, j & 1, abort, p.status))) break;
+            tc_fence_after();
+            if (lane == 0) issue_pv(j);
             __syncwarp();
         }
         if (*abort) {
@@ -272,140 +292,117 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int t = warp >> 2;
-        const int wq = warp & 3;
-        if (active(t)) {
-            const int row_local = wq * 32 + lane;
-            const int row = q0(t) + row_local;
-            const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-            const uint32_t tS = tmem + lane_off + t * 128;
-            const uint32_t tO = tmem + lane_off + 256 + t * 128;
-            const float c = p.c;
-            const int key_lim = p.causal ? min(row, S - 1) : S - 1;
-            float m_use = -INFINITY;
-            float l_sum = 0.f;
-            bool ok = true;
-            for (int j = 0; j <= jmax(t); ++j) {
-                if (!(ok = warp_wait(s_full(t), j & 1, abort, p.status))) break;
-                tc_fence_after();
-                // Pass 1: row max over the tile, 64 columns at a time (keeps
-                // register use within the 168 per thread that ten warps allow).
-                // Only the diagonal tile of a causal row block and a ragged
-                // last tile need the per-element mask; masked scores become
-                // -inf, which exp2 maps to 0 in pass 2.
-                const int kbase = j * BN;
-                const bool mask_tile = (p.causal && j == jmax(t)) || (kbase + BN > S);
-                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        const int h = warp >> 2;                 // column half of every score tile
+        const int wq = warp & 3;                 // lane quarter of Tensor Memory
+        const int row_local = wq * 32 + lane;
+        const int row = q0 + row_local;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const float c = p.c;
+        const int key_lim = p.causal ? min(row, S - 1) : S - 1;
+        float m_use = -INFINITY;
+        float l_part = 0.f;                       // this half's share of the row sum
+        bool ok = true;
+        for (int j = 0; j <= jmax; ++j) {
+            const int b = j & 1;
+            if (!(ok = warp_wait(s_full(b), (j >> 1) & 1, abort, p.status))) break;
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + (uint32_t)b * 128;
+            uint32_t r[64];
+            tmem_ld32(tS + 64 * h, r);
+            tmem_ld32(tS + 64 * h + 32, r + 32);
+            tmem_wait_ld();
+            reg_fence<64>(r);
+            // Only the diagonal tile of a causal row block and a ragged last
+            // tile need the per-element mask; masked scores become -inf.
+            const int kbase = j * BN + 64 * h;
+            if ((p.causal && j == jmax) || (j * BN + BN > S)) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t r[64];
-                    tmem_ld32(tS + 64 * h, r);
-                    tmem_ld32(tS + 64 * h + 32, r + 32);
-                    tmem_wait_ld();
-                    reg_fence<64>(r);
-                    if (mask_tile) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (kbase + 64 * h + i > key_lim) r[i] = 0xff800000u;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 64; i += 8) {
-                        mx0 = max3f(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                        mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                        mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-                        mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
-                    }
-                }
-                const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
-                const float m_tile = mx * c;
-                const float m_new = fmaxf(m_use, m_tile);
-                if (j == 0) {
-                    m_use = m_new;
-                } else {
-                    const bool need = m_new > m_use + RESCALE_THRESHOLD;
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? ex2(m_use - m_new) : 1.f;
-                        if (need) {
-                            l_sum *= alpha;
-                            m_use = m_new;
-                        }
-                        const uint64_t a2 = f2pack(alpha, alpha);
-                        // O is idle here: the PV product of the previous tile
-                        // completed before this tile's S product (issue order).
-#pragma unroll
-                        for (int cb = 0; cb < D; cb += 64) {
-                            constexpr int W = D < 64 ? D : 64;
-                            const int n = (D - cb) < W ? (D - cb) : W;
-                            uint32_t o[64];
-#pragma unroll
-                            for (int u = 0; u < W / 16; ++u)
-                                if (16 * u < n) tmem_ld16(tO + cb + 16 * u, o + 16 * u);
-                            tmem_wait_ld();
-                            reg_fence<64>(o);
-#pragma unroll
-                            for (int i = 0; i < W; i += 2) {
-                                if (i < n) {
-                                    float lo, hi;
-                                    f2unpack(mul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
-                                    o[i] = __float_as_uint(lo);
-                                    o[i + 1] = __float_as_uint(hi);
-                                }
-                            }
-#pragma unroll
-                            for (int u = 0; u < W / 16; ++u)
-                                if (16 * u < n) tmem_st16(tO + cb + 16 * u, o + 16 * u);
-                        }
-                    }
-                }
-                const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
-                const uint64_t c2 = f2pack(c, c);
-                const uint64_t n2 = f2pack(neg, neg);
-                // Pass 2: P = exp2(S*c - m) rounded to bf16 into the first 64
-                // columns of S (columns already read), and its fp32 row sum.
-                uint64_t sum_a = f2pack(0.f, 0.f), sum_b = f2pack(0.f, 0.f);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t r[64];
-                    tmem_ld32(tS + 64 * h, r);
-                    tmem_ld32(tS + 64 * h + 32, r + 32);
-                    tmem_wait_ld();
-                    reg_fence<64>(r);
-                    if (mask_tile) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (kbase + 64 * h + i > key_lim) r[i] = 0xff800000u;
-                    }
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x0, x1;
-                        f2unpack(fma2(f2pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, n2), x0, x1);
-                        const float p0 = ex2(x0);
-                        const float p1 = ex2(x1);
-                        if (i & 1) sum_b = add2(sum_b, f2pack(p0, p1));
-                        else sum_a = add2(sum_a, f2pack(p0, p1));
-                        pk[i] = pack_bf16(p0, p1);
-                    }
-                    tmem_st32(tS + 32 * h, pk);
-                }
-                float s0, s1, s2, s3;
-                f2unpack(sum_a, s0, s1);
-                f2unpack(sum_b, s2, s3);
-                const float sum = (s0 + s1) + (s2 + s3);
-                l_sum += sum;
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(p_full(t));
+                for (int i = 0; i < 64; ++i)
+                    if (kbase + i > key_lim) r[i] = 0xff800000u;
             }
-            // Epilogue (Algorithm 1 lines 15-18).
-            if (ok && warp_wait(o_full(t), 0, abort, p.status)) {
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) {
+                mx0 = max3f(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+            }
+            const float pmax = max3f(mx0, mx1, fmaxf(mx2, mx3));
+            const uint32_t xm = xmax + (uint32_t)(b * 2 * BM) * 8;
+            const float omax = exchange_with_partner(xm + (uint32_t)(h * BM + row_local) * 8,
+                                                     xm + (uint32_t)((1 - h) * BM + row_local) * 8, pmax, j, abort,
+                                                     p.status, ok);
+            if (!ok) break;
+            const float mx = fmaxf(pmax, omax);
+            const float m_new = fmaxf(m_use, mx * c);
+            const float alpha = (j == 0 || m_new == m_use) ? 1.f : ex2(m_use - m_new);
+            m_use = m_new;
+            const float neg = (m_use == -INFINITY) ? 0.f : -m_use;
+            const uint64_t c2 = f2pack(c, c);
+            const uint64_t n2 = f2pack(neg, neg);
+            // P = exp2(S*c - m) rounded to bf16 into columns [32h, 32h+32) of
+            // the score buffer (both halves have read their scores: the
+            // exchange above ordered it), and this half's fp32 row sum.
+            uint64_t sum_a = f2pack(0.f, 0.f), sum_b = f2pack(0.f, 0.f);
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float x0, x1;
+                f2unpack(fma2(f2pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, n2), x0, x1);
+                const float p0 = ex2(x0);
+                const float p1 = ex2(x1);
+                if (i & 1) sum_b = add2(sum_b, f2pack(p0, p1));
+                else sum_a = add2(sum_a, f2pack(p0, p1));
+                pk[i] = pack_bf16(p0, p1);
+            }
+            tmem_st32(tS + 32 * h, pk);
+            float s0, s1, s2, s3;
+            f2unpack(sum_a, s0, s1);
+            f2unpack(sum_b, s2, s3);
+            l_part = l_part * alpha + ((s0 + s1) + (s2 + s3));
+            // Rescale this half's O columns once the previous PV product has
+            // landed (it was issued when the previous P was published).
+            if (j > 0) {
+                if (!(ok = warp_wait(o_done, (j - 1) & 1, abort, p.status))) break;
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    tc_fence_after();
+                    const uint64_t a2 = f2pack(alpha, alpha);
+#pragma unroll
+                    for (int u = h; u < D / 16; u += 2) {
+                        uint32_t o[16];
+                        tmem_ld16(tmem + lane_off + TM_O + 16 * u, o);
+                        tmem_wait_ld();
+                        reg_fence<16>(o);
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            float lo, hi;
+                            f2unpack(mul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
+                            o[i] = __float_as_uint(lo);
+                            o[i + 1] = __float_as_uint(hi);
+                        }
+                        tmem_st16(tmem + lane_off + TM_O + 16 * u, o);
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        // Epilogue (Algorithm 1 lines 15-18): O / l and L = (m + log2 l) ln 2.
+        if (ok) {
+            const float l_other = exchange_with_partner(xl + (uint32_t)(h * BM + row_local) * 8,
+                                                        xl + (uint32_t)((1 - h) * BM + row_local) * 8, l_part, 0,
+                                                        abort, p.status, ok);
+            const float l_sum = l_part + l_other;
+            if (ok && warp_wait(o_done, jmax & 1, abort, p.status)) {
                 tc_fence_after();
                 const float inv = 1.f / l_sum;
                 __nv_bfloat16* orow = p.o + ((size_t)bh * S + row) * D;
 #pragma unroll
-                for (int cc = 0; cc < D / 16; ++cc) {
+                for (int u = h; u < D / 16; u += 2) {
                     uint32_t o[16];
-                    tmem_ld16(tO + 16 * cc, o);
+                    tmem_ld16(tmem + lane_off + TM_O + 16 * u, o);
                     tmem_wait_ld();
                     reg_fence<16>(o);
                     uint32_t pk[8];
@@ -413,12 +410,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
                     for (int i = 0; i < 8; ++i)
                         pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
                     if (row < S) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * cc);
+                        uint4* dst = reinterpret_cast<uint4*>(orow + 16 * u);
                         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
                 }
-                if (row < S) p.lse[(size_t)bh * S + row] = (m_use + log2f(l_sum)) * FA_LN2;
+                if (h == 0 && row < S) p.lse[(size_t)bh * S + row] = (m_use + log2f(l_sum)) * FA_LN2;
             }
         }
     }
@@ -447,7 +444,7 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
     p.lse = a.lse;
     p.status = a.status;
     p.S = a.S;
-    p.n_pairs = (a.S + 2 * BM - 1) / (2 * BM);
+    p.n_qt = (a.S + BM - 1) / BM;
     p.n_kv = (a.S + BN - 1) / BN;
     p.causal = a.causal;
     float c = fabsf(a.scale) * FA_LOG2E;
@@ -456,7 +453,7 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
     auto kern = fwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_pairs, BH);
+    dim3 grid(p.n_qt, BH);
     kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
     return cudaGetLastError();
 }
