@@ -12,15 +12,18 @@
 //   dK  += dS^T Q_i                (Eq. 19; dS^T from shared memory)
 //   dQ_i = dS K                    (Eq. 18; the same shared-memory dS^T tile
 //                                   read as an M-major operand)
-// dQ_i leaves Tensor Memory through a separate warpgroup that adds it into the
-// fp32 dQ accumulator with vector atomics (the stated dQ strategy); the scale
-// of Eq. 18 is applied when the accumulator is converted, that of Eq. 19 when
-// dK is written.
+// dQ_i leaves Tensor Memory through a separate warpgroup: it stages the fp32
+// tile in shared memory (in the slot of Q_i / dO_i, which the products no
+// longer need) and adds it into the fp32 dQ accumulator with TMA bulk
+// reduce-adds, whole 128-byte lines at a time (the stated dQ strategy: atomic
+// accumulation across key tiles).  The scale of Eq. 18 is applied when the
+// accumulator is converted, that of Eq. 19 when dK is written.
 //
-// Warp roles: warps 0-3 scores/softmax/dS (one thread per key row) and the
-// final dK/dV store, warps 4-7 the dQ read-out and atomics (one thread per
-// query row), warp 8 TMA (K, V once; Q_i, dO_i per tile, plus L and D), warp 9
-// Tensor Memory allocation and the single-thread MMA issuer.
+// Warp roles: warps 0-7 P^T and dS^T (one thread per key row; warps 0-3 take
+// query columns 0-63, warps 4-7 columns 64-127) and the final dK/dV store,
+// warps 8-11 the dQ read-out (one thread per query row), warp 12 TMA (K, V
+// once; Q_i, dO_i per tile, plus L and D), warp 13 Tensor Memory allocation
+// and the single-thread MMA issuer.
 // Tensor Memory columns: dV [0,128), dK [128,256), S^T/P^T [256,384),
 // dP^T [384,512), which dQ_i reuses once dS^T has been formed.
 
@@ -40,9 +43,10 @@ using namespace tc;
 
 constexpr int BK = 128;
 constexpr int BQ = 128;
-constexpr int NTHREADS = 320;
-constexpr int TMA_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int NTHREADS = 448;
+constexpr int DQ_WARP0 = 8;
+constexpr int TMA_WARP = 12;
+constexpr int MMA_WARP = 13;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
 constexpr int SMEM_BUDGET = 227 * 1024;
@@ -53,18 +57,17 @@ struct BwdCfg {
     static constexpr int DS_BYTES = BK * BQ * 2;
     static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
     static constexpr int FIXED = 2 * TILE + DS_BYTES;  // K, V, dS^T
-    static constexpr int STAGE = 2 * TILE + LD_BYTES;  // Q_i, dO_i, (L, D)_i
+    static constexpr int STAGE = 2 * TILE + LD_BYTES;  // [Q_i | dO_i], (L, D)_i
     static constexpr int NS_RAW = (SMEM_BUDGET - FIXED - 256) / STAGE;
     static constexpr int NS = NS_RAW > 3 ? 3 : NS_RAW;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = TILE;
     static constexpr int DS_OFF = 2 * TILE;
-    static constexpr int Q_OFF = DS_OFF + DS_BYTES;
-    static constexpr int DO_OFF = Q_OFF + NS * TILE;
-    static constexpr int LD_OFF = DO_OFF + NS * TILE;
+    static constexpr int QD_OFF = DS_OFF + DS_BYTES;   // stage s: Q at QD_OFF + 2*TILE*s, dO right after
+    static constexpr int LD_OFF = QD_OFF + NS * 2 * TILE;
     static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
-    // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, done, drain
-    static constexpr int NBARS = 7 + 2 * NS;
+    // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain
+    static constexpr int NBARS = 8 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -72,14 +75,27 @@ struct BwdCfg {
     static_assert(BYTES <= SMEM_BUDGET, "shared memory budget");
 };
 
+// fp32 dQ tile [128 rows][d] staged for TMA as 32-column boxes (128-byte
+// rows, 128-byte swizzle) plus one 16-column box (64-byte rows, 64-byte
+// swizzle) when d is not a multiple of 32.  128 * d * 4 bytes = the Q_i + dO_i
+// slot it is staged in.
+template <int D>
+struct DqChunks {
+    static constexpr int N32 = D / 32;
+    static constexpr int NCH = N32 + (D % 32 ? 1 : 0);
+    __host__ __device__ static constexpr int width(int c) { return c < N32 ? 32 : 16; }
+    __host__ __device__ static constexpr int map_index(int c) { return c < N32 ? 0 : 1; }
+    __host__ __device__ static constexpr int offset(int c) { return c * 128 * 128; }
+};
+
 struct BwdParams {
     CUtensorMap tq[2];
     CUtensorMap tk[2];
     CUtensorMap tv[2];
     CUtensorMap tdo[2];
+    CUtensorMap tdq[2];
     const float* lse;
     const float* Dvec;
-    float* dQacc;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     unsigned int* status;
@@ -99,10 +115,6 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
-}
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // B operand of the products whose N dimension is the head dim: a [rows][d]
@@ -149,6 +161,7 @@ __device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_lo, uint3
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
     using C = Chunks<D>;
+    using QC = DqChunks<D>;
     using G = BwdCfg<D>;
     constexpr int NS = G::NS;
 
@@ -169,10 +182,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t p_full = s_full + 8;
     const uint32_t dq_full = s_full + 16;
     const uint32_t dq_empty = s_full + 24;
-    const uint32_t done = s_full + 32;
-    const uint32_t drain = s_full + 40;
+    const uint32_t stg = s_full + 32;
+    const uint32_t done = s_full + 40;
+    const uint32_t drain = s_full + 48;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
+    auto q_slot = [&](int s) { return sb + G::QD_OFF + (uint32_t)(s * 2 * G::TILE); };
+    auto do_slot = [&](int s) { return sb + G::QD_OFF + (uint32_t)(s * 2 * G::TILE + G::TILE); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -187,12 +203,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(kv_full, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(q_full(s), 33);        // TMA expect-tx arrival + 32 lanes that stage (L, D)
-            mbar_init(q_empty(s), 1);
+            mbar_init(q_empty(s), 1);        // the dQ warpgroup, once the slot's staging has been read
         }
         mbar_init(s_full, 1);
-        mbar_init(p_full, BK);
+        mbar_init(p_full, 2 * BK);
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, BQ);
+        mbar_init(stg, BQ);
         mbar_init(done, 1);
         mbar_init(drain, 1);
         *abort = 0;
@@ -234,10 +251,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mbar_arrive_expect_tx(q_full(s), 2 * G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_3d(sb + G::Q_OFF + s * G::TILE + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64,
-                                q0, bh, q_full(s));
-                    tma_load_3d(sb + G::DO_OFF + s * G::TILE + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64,
-                                q0, bh, q_full(s));
+                    tma_load_3d(q_slot(s) + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64, q0, bh, q_full(s));
+                    tma_load_3d(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64, q0, bh, q_full(s));
                 }
             }
             // (L * log2 e, D) for the 128 query rows; rows past S get (+inf, 0) so P = 0.
@@ -269,8 +284,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         // [rows][d] tiles use the 64-column chunk stride as LBO.
         const uint32_t k_lo = desc_lo(sb + G::K_OFF, 16), v_lo = desc_lo(sb + G::V_OFF, 16);
         const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, 128 * 128);
-        const uint32_t q_lo0 = desc_lo(sb + G::Q_OFF, 16), do_lo0 = desc_lo(sb + G::DO_OFF, 16);
-        const uint32_t q_mn_lo0 = desc_lo(sb + G::Q_OFF, 128 * 128), do_mn_lo0 = desc_lo(sb + G::DO_OFF, 128 * 128);
+        const uint32_t q_lo0 = desc_lo(sb + G::QD_OFF, 16), do_lo0 = desc_lo(sb + G::QD_OFF + G::TILE, 16);
+        const uint32_t q_mn_lo0 = desc_lo(sb + G::QD_OFF, 128 * 128);
+        const uint32_t do_mn_lo0 = desc_lo(sb + G::QD_OFF + G::TILE, 128 * 128);
         const uint32_t ds_k_lo = desc_lo(sb + G::DS_OFF, 16);          // dS^T as K-major A (dK)
         const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);       // dS as M-major A (dQ)
         const uint32_t ds_hi = desc_hi(1024, SW_128B);
@@ -278,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         for (int it = 0; it < n_it && ok; ++it) {
             const int s = it % NS;
             const uint32_t ph = (it / NS) & 1;
-            const uint32_t so = (uint32_t)s * (G::TILE >> 4);
+            const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
             if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);         // S^T = K Q^T
@@ -291,10 +307,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) {
+                // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)                                        // dV += P^T dO
-                    mma_n_is_d<D, true>(tmem + TM_DV, tmem + TM_S + ks * 8, 0, do_mn_lo0 + so, ks, 0,
-                                        (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_n_is_d<D, true>(tmem + TM_DV, tmem + TM_S + (ks / 4) * 64 + (ks % 4) * 8, 0, do_mn_lo0 + so,
+                                        ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
                     const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
@@ -306,7 +323,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     mma_n_is_d<D, false>(tmem + TM_DP, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(dq_full);
-                mma_commit(q_empty(s));
             }
             __syncwarp();
         }
@@ -319,12 +335,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < DQ_WARP0) {
         // ------------------------------------------------------------ P^T, dS^T and the dK/dV store
-        const int jr = warp * 32 + lane;               // key row inside the tile
+        const int h = warp >> 2;                       // query columns [64h, 64h+64)
+        const int wq = warp & 3;
+        const int jr = wq * 32 + lane;                 // key row inside the tile
         const int key = k0 + jr;
         const bool key_ok = key < S;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + TM_S;
         const uint32_t tP = tmem + lane_off + TM_DP;
         const float c = p.c;
@@ -340,7 +358,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_after();
             const uint32_t ldb = sb + G::LD_OFF + s * G::LD_BYTES;
 #pragma unroll
-            for (int qq = 0; qq < BQ / 32; ++qq) {
+            for (int qh = 0; qh < 2; ++qh) {
+                const int qq = 2 * h + qh;                                  // 32-query quarter of the tile
                 uint32_t rs[32], rp[32];
                 tmem_ld32(tS + 32 * qq, rs);
                 tmem_ld32(tP + 32 * qq, rp);
@@ -361,13 +380,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     pk[e] = pack_bf16(p0, p1);
                     dk[e] = pack_bf16(d0, d1);
                 }
-                tmem_st16(tS + 16 * qq, pk);
+                // P^T of these 32 queries into 16 columns of this half's own
+                // (already read) score columns.
+                tmem_st16(tS + 64 * h + 16 * qh, pk);
                 // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
                 // 128-byte-swizzled [key][query] tile (two 64-query chunks).
-                const uint32_t chunk = ds_row + (uint32_t)(qq >> 1) * 16384;
+                const uint32_t chunk = ds_row + (uint32_t)h * 16384;
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
-                    const uint32_t u = (uint32_t)((qq & 1) * 4 + u4);
+                    const uint32_t u = (uint32_t)(qh * 4 + u4);
                     st_shared_v4(chunk + ((u ^ swz) << 4), dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
                 }
             }
@@ -376,12 +397,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(p_full);
         }
-        // dK, dV rows of this key tile.
+        // dK, dV rows of this key tile (16-column units split between the halves).
         if (ok && warp_wait(done, 0, abort, p.status)) {
             tc_fence_after();
             const size_t row = (size_t)bh * S + key;
 #pragma unroll
-            for (int u = 0; u < D / 16; ++u) {
+            for (int u = h; u < D / 16; u += 2) {
                 uint32_t a[16], b[16];
                 tmem_ld16(tmem + lane_off + TM_DV + 16 * u, a);
                 tmem_ld16(tmem + lane_off + TM_DK + 16 * u, b);
@@ -405,29 +426,63 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             }
         }
     } else {
-        // ------------------------------------------------------------ dQ_i read-out and atomics
+        // ------------------------------------------------------------ dQ_i read-out and reduce-add
         const int wq = warp & 3;
         const int qr = wq * 32 + lane;                 // query row inside the tile
         const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM_DP;
+        const bool leader = threadIdx.x == DQ_WARP0 * 32;
         for (int it = 0; it < n_it; ++it) {
+            const int s = it % NS;
             if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
             tc_fence_after();
-            const int q = (i0 + it) * BQ + qr;
-            float* dst = p.dQacc + ((size_t)bh * S + q) * D;
-            uint32_t r[D];
+            // Stage this row into the Q_i / dO_i slot (the products that read
+            // them finished before dQ_i did), box by box in the TMA swizzle.
+            const uint32_t slot = q_slot(s);
 #pragma unroll
-            for (int u = 0; u < D / 16; ++u) tmem_ld16(tQ + 16 * u, r + 16 * u);
-            tmem_wait_ld();
-            reg_fence<D>(r);
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-            if (q < S) {
+            for (int cq = 0; cq < QC::NCH; ++cq) {
+                constexpr int W32 = 32;
+                const int w = QC::width(cq);
+                uint32_t r[W32];
+                if (w == 32) tmem_ld32(tQ + 32 * cq, r);
+                else tmem_ld16(tQ + 32 * cq, r);
+                tmem_wait_ld();
+                reg_fence<W32>(r);
+                if (cq == QC::NCH - 1) {
+                    tc_fence_before();
+                    mbar_arrive(dq_empty);                 // TMEM columns free for the next dP^T
+                }
+                const uint32_t rb = (uint32_t)w * 4;       // 128 or 64 bytes per row
+                const uint32_t mask = w == 32 ? 7u : 3u;
+                const uint32_t base = slot + QC::offset(cq);
 #pragma unroll
-                for (int u = 0; u < D / 4; ++u)
-                    red_add_v4(dst + 4 * u, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                               __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+                for (int u = 0; u < W32 / 4; ++u) {
+                    if (u < w / 4) {
+                        const uint32_t off = (uint32_t)qr * rb + (uint32_t)u * 16;
+                        const uint32_t phys = off ^ (((off >> 7) & mask) << 4);
+                        st_shared_v4(base + phys, r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+                    }
+                }
             }
+            fence_proxy_async_smem();
+            mbar_arrive(stg);
+            int lead_ok = 1;
+            if (leader) {
+                if (mbar_wait(stg, it & 1, abort, p.status, WAIT_LIMIT_NS)) {
+                    const int q0 = (i0 + it) * BQ;
+#pragma unroll
+                    for (int cq = 0; cq < QC::NCH; ++cq)
+                        tma_reduce_add_3d(&p.tdq[QC::map_index(cq)], slot + QC::offset(cq), cq * 32, q0, bh);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(q_empty(s));               // the slot may take the next Q / dO tile
+                } else {
+                    lead_ok = 0;
+                }
+            }
+            // The whole warp leaves together if the leader gave up.
+            if ((warp == DQ_WARP0) && __shfl_sync(0xffffffffu, lead_ok, 0) == 0) break;
         }
+        if (leader) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -450,9 +505,14 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
         if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, 128)) != cudaSuccess) return e;
         if (C::REM > 0 && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess) return e;
     }
+    {
+        using QC = DqChunks<D>;
+        cudaError_t e;
+        if (QC::N32 > 0 && (e = make_tmap_f32_3d(&p.tdq[0], a.dQacc, D, a.S, BH, 32, 128)) != cudaSuccess) return e;
+        if (QC::NCH > QC::N32 && (e = make_tmap_f32_3d(&p.tdq[1], a.dQacc, D, a.S, BH, 16, 128)) != cudaSuccess) return e;
+    }
     p.lse = a.lse;
     p.Dvec = a.Dvec;
-    p.dQacc = a.dQacc;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.status = a.status;

@@ -13,4 +13,8 @@ namespace fa {
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w,
                               int box_rows);
 
+// Same over a contiguous [BH, S, d] fp32 array (box inner extent 64 or 128
+// bytes, matching swizzle), used to reduce-add tiles into it.
+cudaError_t make_tmap_f32_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w, int box_rows);
+
 }  // namespace fa
