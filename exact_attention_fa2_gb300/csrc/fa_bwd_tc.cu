@@ -48,26 +48,47 @@ constexpr int DQ_WARP0 = 8;
 constexpr int TMA_WARP = 12;
 constexpr int MMA_WARP = 13;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 384;
+constexpr uint32_t TM_S = 256, TM_DP = 384;
 constexpr int SMEM_BUDGET = 227 * 1024;
+
+// Tensor Memory columns.  For d <= 64 every product has its own columns
+// (dV, dK, dQ_i, the bf16 P^T pairs, S^T, dP^T): S^T and dP^T of the next
+// query tile are computed while the softmax warps still work on this one, and
+// the dV/dK/dQ products of this tile run while they work on the next.  For
+// larger d the accumulators leave no room: P^T overwrites S^T, dQ_i reuses
+// dP^T, and the products of consecutive tiles follow each other.
+template <int D>
+struct BwdTm {
+    static constexpr bool PIPE = D <= 64;
+    static constexpr uint32_t DV = 0;
+    static constexpr uint32_t DK = PIPE ? 64 : 128;
+    static constexpr uint32_t DQ = PIPE ? 128 : TM_DP;
+    static constexpr uint32_t P = PIPE ? 192 : TM_S;
+    // Column of P^T for query columns [64h + 32qh, 64h + 32qh + 32) (16 pairs).
+    __device__ static constexpr uint32_t p_col(int h, int qh) { return PIPE ? P + 32 * h + 16 * qh : P + 64 * h + 16 * qh; }
+    // A operand (16 queries) of k-step ks of dV += P^T dO.
+    __device__ static constexpr uint32_t p_kstep(int ks) { return PIPE ? P + 8 * ks : P + (ks / 4) * 64 + (ks % 4) * 8; }
+};
 
 template <int D>
 struct BwdCfg {
     static constexpr int TILE = 128 * D * 2;
     static constexpr int DS_BYTES = BK * BQ * 2;
+    static constexpr int NDS = BwdTm<D>::PIPE ? 2 : 1;      // dS^T buffers
     static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
-    static constexpr int FIXED = 2 * TILE + DS_BYTES;  // K, V, dS^T
+    static constexpr int FIXED = 2 * TILE + NDS * DS_BYTES;  // K, V, dS^T
     static constexpr int STAGE = 2 * TILE + LD_BYTES;  // [Q_i | dO_i], (L, D)_i
     static constexpr int NS_RAW = (SMEM_BUDGET - FIXED - 256) / STAGE;
     static constexpr int NS = NS_RAW > 3 ? 3 : NS_RAW;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = TILE;
     static constexpr int DS_OFF = 2 * TILE;
-    static constexpr int QD_OFF = DS_OFF + DS_BYTES;   // stage s: Q at QD_OFF + 2*TILE*s, dO right after
+    static constexpr int QD_OFF = DS_OFF + NDS * DS_BYTES;   // stage s: Q at QD_OFF + 2*TILE*s, dO right after
     static constexpr int LD_OFF = QD_OFF + NS * 2 * TILE;
     static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
-    // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain
-    static constexpr int NBARS = 8 + 2 * NS;
+    // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain,
+    // s_free, p_free, ds_free[2]
+    static constexpr int NBARS = 12 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -101,6 +122,7 @@ struct BwdParams {
     unsigned int* status;
     int S;
     int n_q;
+    int n_kv;
     int causal;
     float c;          // |scale| * log2(e), at least 1e-30
     float scale;      // signed scale applied to dK
@@ -185,6 +207,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t stg = s_full + 32;
     const uint32_t done = s_full + 40;
     const uint32_t drain = s_full + 48;
+    const uint32_t s_free = s_full + 56;      // S^T and dP^T have been read (pipelined schedule)
+    const uint32_t p_free = s_full + 64;      // dV has read P^T
+    auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dK and dQ have read dS^T buffer b
+    using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
     auto q_slot = [&](int s) { return sb + G::QD_OFF + (uint32_t)(s * 2 * G::TILE); };
@@ -192,8 +218,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int j = blockIdx.x;                 // key tile; early tiles see the most query tiles
-    const int bh = blockIdx.y;
+    // One flat grid ordered key-tile-major: early key tiles see the most query
+    // tiles under the causal mask, so every head's heaviest tile goes first.
+    const int BH = (int)(gridDim.x / (unsigned)p.n_kv);
+    const int j = (int)blockIdx.x / BH;
+    const int bh = (int)blockIdx.x - j * BH;
     const int S = p.S;
     const int k0 = j * BK;
     const int i0 = p.causal ? j : 0;          // query tiles above the diagonal are fully masked
@@ -212,6 +241,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(stg, BQ);
         mbar_init(done, 1);
         mbar_init(drain, 1);
+        mbar_init(s_free, 2 * BK);
+        mbar_init(p_free, 1);
+        mbar_init(ds_free(0), 1);
+        mbar_init(ds_free(1), 1);
         *abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -291,7 +324,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);       // dS as M-major A (dQ)
         const uint32_t ds_hi = desc_hi(1024, SW_128B);
         bool ok = warp_wait(kv_full, 0, abort, p.status);
-        for (int it = 0; it < n_it && ok; ++it) {
+        if constexpr (TM::PIPE) {
+            // S^T, dP^T of tile it+1 go in as soon as the softmax warps have
+            // read those of tile it; dV, dK, dQ of tile it once P^T, dS^T exist.
+            auto issue_sdp = [&](int it) {
+                const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
+                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
+                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);               // dP^T = V dO^T
+                mma_commit(s_full);
+            };
+            if (ok) ok = warp_wait(q_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                if (lane == 0) issue_sdp(0);
+                __syncwarp();
+            }
+            for (int it = 0; it < n_it && ok; ++it) {
+                const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
+                const uint32_t dso = (uint32_t)((it & 1) * G::DS_BYTES) >> 4;
+                if (it + 1 < n_it) {
+                    if (!(ok = warp_wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1, abort, p.status))) break;
+                    if (!(ok = warp_wait(s_free, it & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    if (lane == 0) issue_sdp(it + 1);
+                    __syncwarp();
+                }
+                if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int ks = 0; ks < BQ / 16; ++ks)                                  // dV += P^T dO
+                        mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so, ks, 0,
+                                            (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(p_free);
+#pragma unroll
+                    for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
+                        const uint64_t adesc =
+                            desc_make(ds_k_lo + dso + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
+                        mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
+                                             (it > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
+                        const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, ds_hi);
+                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(dq_full);
+                    mma_commit(ds_free(it & 1));
+                }
+                __syncwarp();
+            }
+        }
+        for (int it = 0; it < n_it && ok && !TM::PIPE; ++it) {
             const int s = it % NS;
             const uint32_t ph = (it / NS) & 1;
             const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
@@ -310,17 +398,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_n_is_d<D, true>(tmem + TM_DV, tmem + TM_S + (ks / 4) * 64 + (ks % 4) * 8, 0, do_mn_lo0 + so,
+                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
                                         ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
                     const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM_DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {                                      // dQ_i = dS K
                     const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM_DP, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(dq_full);
             }
@@ -366,6 +454,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 tmem_wait_ld();
                 reg_fence<32>(rs);
                 reg_fence<32>(rp);
+                if (TM::PIPE && qh == 1) {
+                    tc_fence_before();
+                    mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
+                }
                 uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -380,18 +472,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     pk[e] = pack_bf16(p0, p1);
                     dk[e] = pack_bf16(d0, d1);
                 }
-                // P^T of these 32 queries into 16 columns of this half's own
-                // (already read) score columns.
-                tmem_st16(tS + 64 * h + 16 * qh, pk);
+                if (TM::PIPE && qh == 0) {
+                    // P^T and dS^T buffers of earlier tiles must have been read.
+                    if (it > 0 && !(ok = warp_wait(p_free, (it - 1) & 1, abort, p.status))) break;
+                    if (it > 1 && !(ok = warp_wait(ds_free(it & 1), ((it >> 1) - 1) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                }
+                // P^T of these 32 queries: 16 columns of bf16 pairs (for
+                // d > 64 inside this half's own, already read, score columns).
+                tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
                 // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
                 // 128-byte-swizzled [key][query] tile (two 64-query chunks).
-                const uint32_t chunk = ds_row + (uint32_t)h * 16384;
+                const uint32_t chunk = ds_row + (uint32_t)((it & 1) * (G::NDS - 1) * G::DS_BYTES) + (uint32_t)h * 16384;
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
                     const uint32_t u = (uint32_t)(qh * 4 + u4);
                     st_shared_v4(chunk + ((u ^ swz) << 4), dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
                 }
             }
+            if (!ok) break;
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -404,8 +503,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
 #pragma unroll
             for (int u = h; u < D / 16; u += 2) {
                 uint32_t a[16], b[16];
-                tmem_ld16(tmem + lane_off + TM_DV + 16 * u, a);
-                tmem_ld16(tmem + lane_off + TM_DK + 16 * u, b);
+                tmem_ld16(tmem + lane_off + TM::DV + 16 * u, a);
+                tmem_ld16(tmem + lane_off + TM::DK + 16 * u, b);
                 tmem_wait_ld();
                 reg_fence<16>(a);
                 reg_fence<16>(b);
@@ -429,7 +528,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         // ------------------------------------------------------------ dQ_i read-out and reduce-add
         const int wq = warp & 3;
         const int qr = wq * 32 + lane;                 // query row inside the tile
-        const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM_DP;
+        const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM::DQ;
         const bool leader = threadIdx.x == DQ_WARP0 * 32;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % NS;
@@ -518,6 +617,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     p.status = a.status;
     p.S = a.S;
     p.n_q = (a.S + BQ - 1) / BQ;
+    p.n_kv = (a.S + BK - 1) / BK;
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;
@@ -526,7 +626,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     auto kern = bwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.S + BK - 1) / BK, BH);
+    dim3 grid(p.n_kv * BH);
     kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
     return cudaGetLastError();
 }

@@ -134,8 +134,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int qt = p.causal ? (p.n_qt - 1 - (int)blockIdx.x) : (int)blockIdx.x;   // long rows first
-    const int bh = blockIdx.y;
+    // One flat grid ordered tile-rank-major: every head's longest causal row
+    // block is dispatched before any head's next one (longest job first).
+    const int BH = (int)(gridDim.x / (unsigned)p.n_qt);
+    const int rank = (int)blockIdx.x / BH;
+    const int bh = (int)blockIdx.x - rank * BH;
+    const int qt = p.causal ? (p.n_qt - 1 - rank) : rank;
     const int S = p.S;
     const int q0 = qt * BM;
     const int jmax = p.causal ? min(qt, p.n_kv - 1) : p.n_kv - 1;   // key tiles 0..jmax
@@ -453,7 +457,7 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
     auto kern = fwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_qt, BH);
+    dim3 grid(p.n_qt * BH);
     kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
     return cudaGetLastError();
 }
