@@ -94,6 +94,7 @@ struct BwdCfg {
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
     static_assert(NS >= 2, "Q/dO ring needs two stages");
     static_assert(BYTES <= SMEM_BUDGET, "shared memory budget");
+    static_assert(!BwdTm<D>::PIPE || BQ * D * 4 <= DS_BYTES, "fp32 dQ tile staged in a dS^T buffer");
 };
 
 // fp32 dQ tile [128 rows][d] staged for TMA as 32-column boxes (128-byte
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t drain = s_full + 48;
     const uint32_t s_free = s_full + 56;      // S^T and dP^T have been read (pipelined schedule)
     const uint32_t p_free = s_full + 64;      // dV has read P^T
-    auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dK and dQ have read dS^T buffer b
+    auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dS^T buffer b (holding the staged dQ) is free
     using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
@@ -232,7 +233,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(kv_full, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(q_full(s), 33);        // TMA expect-tx arrival + 32 lanes that stage (L, D)
-            mbar_init(q_empty(s), 1);        // the dQ warpgroup, once the slot's staging has been read
+            // d <= 64: the MMA issuer once dV and dK (the last readers) are issued;
+            // otherwise the dQ warpgroup, once the dQ_i staged in the slot has been read.
+            mbar_init(q_empty(s), 1);
         }
         mbar_init(s_full, 1);
         mbar_init(p_full, 2 * BK);
@@ -364,6 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
                                              (it > 0 || ks > 0) ? 1u : 0u);
                     }
+                    mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
                 }
                 if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
                 tc_fence_after();
@@ -374,7 +378,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(dq_full);
-                    mma_commit(ds_free(it & 1));
                 }
                 __syncwarp();
             }
@@ -534,9 +537,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             const int s = it % NS;
             if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
             tc_fence_after();
-            // Stage this row into the Q_i / dO_i slot (the products that read
-            // them finished before dQ_i did), box by box in the TMA swizzle.
-            const uint32_t slot = q_slot(s);
+            // Stage this row box by box in the TMA swizzle: for d <= 64 into
+            // the dS^T buffer that dK and dQ_i have just read (dQ_i is 32 KB
+            // at most), otherwise into the Q_i / dO_i slot (the products that
+            // read them finished before dQ_i did).
+            const uint32_t slot = TM::PIPE ? sb + G::DS_OFF + (uint32_t)((it & 1) * G::DS_BYTES) : q_slot(s);
 #pragma unroll
             for (int cq = 0; cq < QC::NCH; ++cq) {
                 constexpr int W32 = 32;
@@ -573,7 +578,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         tma_reduce_add_3d(&p.tdq[QC::map_index(cq)], slot + QC::offset(cq), cq * 32, q0, bh);
                     bulk_commit();
                     bulk_wait_read();
-                    mbar_arrive(q_empty(s));               // the slot may take the next Q / dO tile
+                    // The buffer may take the next dS^T / the next Q, dO tile.
+                    mbar_arrive(TM::PIPE ? ds_free(it & 1) : q_empty(s));
                 } else {
                     lead_ok = 0;
                 }
