@@ -271,8 +271,6 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    fa.profile_read()                      # drop anything recorded so far
-    fa.profile_enable(True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -286,11 +284,24 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
-    fa.profile_enable(False)
-    prof = fa.profile_read()
     fa.check_status()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world)
+
+    # Per-kernel device times from a separate pass with the library's timing
+    # events around every launch (they serialise the kernels, so the step
+    # time above is taken without them).
+    prof_steps = max(5, min(args.steps, 50))
+    fa.profile_read()                      # drop anything recorded so far
+    fa.profile_enable(True)
+    for i in range(prof_steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    fa.profile_enable(False)
+    prof = fa.profile_read()
+    fa.check_status()
+    launches_per_step = sum(v[1] for v in prof.values()) / prof_steps
 
     # End to end through the public API with pinned host buffers.
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
@@ -365,7 +376,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peaks['source']} bf16 burst"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": sum(v[1] for v in prof.values()),
+        "gpu_launches": int(round(launches_per_step * args.steps)),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v_cpu, n_sl, el, thr = cpu_oracle_sample(w, args.cpu_seconds)

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_launch();
 
     if (warp == TMA_WARP) {
         // ------------------------------------------------------------ producer
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
             // (L * log2 e, D) for the 128 query rows; rows past S get (+inf, 0) so P = 0.
+            // D (and the zeroed dQ accumulator) come from the previous kernel.
+            if (it == 0) griddep_wait();
             const size_t rb = (size_t)bh * S;
 #pragma unroll
             for (int e = 0; e < BQ / 32; ++e) {
@@ -533,6 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const int qr = wq * 32 + lane;                 // query row inside the tile
         const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM::DQ;
         const bool leader = threadIdx.x == DQ_WARP0 * 32;
+        griddep_wait();                                // the dQ accumulator is zeroed by the previous kernel
         for (int it = 0; it < n_it; ++it) {
             const int s = it % NS;
             if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
@@ -632,9 +636,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     auto kern = bwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_kv * BH);
-    kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.n_kv * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }
 
 }  // namespace

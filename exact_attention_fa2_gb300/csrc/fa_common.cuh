@@ -64,6 +64,12 @@ template <> struct Vec16<__nv_bfloat16> {
     }
 };
 
+// Programmatic dependent launch: wait until the previous kernel on the stream
+// has completed and its writes are visible (returns at once when the kernel
+// was launched without the attribute); let the next kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(unsigned int* status, unsigned int code) {
     if (status) atomicOr(status, code);
 }

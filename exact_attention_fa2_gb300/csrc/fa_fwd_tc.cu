@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_launch();
 
     if (warp == TMA_WARP) {
         // ------------------------------------------------------------ producer
@@ -193,6 +194,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
                 prefetch_tmap(&p.tk[i]);
                 prefetch_tmap(&p.tv[i]);
             }
+            // Q, K, V may come from the previous kernel on the stream; every
+            // global access of this CTA follows these loads.
+            griddep_wait();
             mbar_arrive_expect_tx(q_full, (hasB ? 2 : 1) * G::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
@@ -514,9 +518,7 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
     auto kern = fwd_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_units * BH);
-    kern<<<grid, NTHREADS, G::DYN_SMEM, a.stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.n_units * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }
 
 }  // namespace

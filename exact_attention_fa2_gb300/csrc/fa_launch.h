@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <algorithm>
+
 namespace fa {
 
 enum { DT_BF16 = 0, DT_FP32 = 1 };
@@ -41,6 +43,26 @@ struct BwdArgs {
     cudaStream_t stream;
     unsigned int* status;
 };
+
+// Launch `kern` as a programmatic dependent of the previous kernel on the
+// stream: its blocks may start while that kernel drains and must execute
+// griddepcontrol.wait before reading anything the previous kernel writes (or
+// writing anything it reads).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // fp32 (and generic) FMA-pipe kernels.
 cudaError_t launch_fwd_simt(const FwdArgs& a);
