@@ -279,10 +279,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 tma_load_3d(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], c * 64, k0, bh, kv_full);
             }
         }
+        const size_t rb = (size_t)bh * S;
         for (int it = 0; it < n_it; ++it) {
             const int s = it % NS;
             const uint32_t ph = (it / NS) & 1;
             const int q0 = (i0 + it) * BQ;
+            // (L * log2 e, D) for the 128 query rows, loaded before the stage
+            // is free so that the loads overlap the wait; rows past S get
+            // (+inf, 0) so that P = 0.  D (and the zeroed dQ accumulator)
+            // come from the previous kernel.
+            if (it == 0) griddep_wait();
+            float l2[BQ / 32], dd[BQ / 32];
+#pragma unroll
+            for (int e = 0; e < BQ / 32; ++e) {
+                const int q = q0 + e * 32 + lane;
+                l2[e] = q < S ? p.lse[rb + q] * FA_LOG2E : INFINITY;
+                dd[e] = q < S ? p.Dvec[rb + q] : 0.f;
+            }
             if (!warp_wait(q_empty(s), ph ^ 1, abort, p.status)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(q_full(s), 2 * G::TILE);
@@ -292,19 +305,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     tma_load_3d(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64, q0, bh, q_full(s));
                 }
             }
-            // (L * log2 e, D) for the 128 query rows; rows past S get (+inf, 0) so P = 0.
-            // D (and the zeroed dQ accumulator) come from the previous kernel.
-            if (it == 0) griddep_wait();
-            const size_t rb = (size_t)bh * S;
 #pragma unroll
-            for (int e = 0; e < BQ / 32; ++e) {
-                const int qr = e * 32 + lane;
-                const int q = q0 + qr;
-                const float l2 = q < S ? p.lse[rb + q] * FA_LOG2E : INFINITY;
-                const float dd = q < S ? p.Dvec[rb + q] : 0.f;
-                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(sb + G::LD_OFF + s * G::LD_BYTES + qr * 8),
-                             "f"(l2), "f"(dd) : "memory");
-            }
+            for (int e = 0; e < BQ / 32; ++e)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(sb + G::LD_OFF + s * G::LD_BYTES + (e * 32 + lane) * 8),
+                             "f"(l2[e]), "f"(dd[e]) : "memory");
             mbar_arrive(q_full(s));
             issued = it + 1;
         }
