@@ -82,6 +82,10 @@ def load_library():
         lib.fa_profile_enable.restype = i
         lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
         lib.fa_profile_read.restype = i
+        lib.fa_fwd_bwd_host_buffer_size.argtypes = [i, i, i, i, i]
+        lib.fa_fwd_bwd_host_buffer_size.restype = sz
+        lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_bwd_host.restype = i
         _lib = lib
     return _lib
 
@@ -198,6 +202,42 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
                     B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
     _check(rc)
     return dq, dk, dv
+
+
+def fwd_bwd_host_buffer_size(B: int, H: int, S: int, d: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (FA_BF16 if dtype == torch.bfloat16 else FA_FP32)
+    return int(load_library().fa_fwd_bwd_host_buffer_size(B, H, S, d, code))
+
+
+def fwd_bwd_host(q, k, v, do, out, dev_buf, causal: bool = False, scale=None, stream=None):
+    """One forward + backward step on host tensors (pinned for asynchronous
+    copies): ``out`` = (o, lse, dq, dk, dv) host tensors that receive the
+    results, ``dev_buf`` a uint8 device tensor of at least
+    fwd_bwd_host_buffer_size() bytes.  Returns immediately; the results are
+    valid once ``stream`` (default: the current stream of dev_buf's device)
+    has completed."""
+    for t in (q, k, v, do):
+        if t.is_cuda or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("q, k, v, dO must be contiguous host tensors of one shape and dtype")
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, S, d] tensors")
+    o, lse, dq, dk, dv = out
+    B, H, S, d = q.shape
+    for t in (o, dq, dk, dv):
+        if t.is_cuda or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o, dq, dk, dv must be contiguous host tensors like q")
+    if lse.is_cuda or lse.shape != (B, H, S) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 host tensor of shape [B, H, S]")
+    if not dev_buf.is_cuda:
+        raise ValueError("dev_buf must be a device tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(dev_buf.device):
+        st = _stream_handle(stream)
+        rc = load_library().fa_fwd_bwd_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(dev_buf), dev_buf.numel() * dev_buf.element_size(), B, H, S, d, int(causal), scale,
+            _dtype_code(q), ctypes.c_void_p(st))
+    _check(rc)
 
 
 class FlashAttention(torch.autograd.Function):

@@ -11,7 +11,9 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 namespace {
@@ -124,6 +126,43 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
     return e;
 }
 
+// One non-blocking helper stream per (device, caller stream), created on first
+// use by fa_fwd_bwd_host and kept for the life of the process.
+std::mutex g_side_mu;
+std::map<std::pair<int, void*>, cudaStream_t> g_side;
+
+int side_stream(void* user, cudaStream_t* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    auto it = g_side.find({dev, user});
+    if (it == g_side.end()) {
+        cudaStream_t st = nullptr;
+        e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+        it = g_side.emplace(std::make_pair(dev, user), st).first;
+    }
+    *out = it->second;
+    return FA_OK;
+}
+
+// Device layout of fa_fwd_bwd_host's buffer: q, k, v, dO, o, dq, dk, dv, lse,
+// then the backward workspace, each starting on a 256-byte boundary.
+struct HostStepLayout {
+    size_t arr, lse, ws, total;
+};
+HostStepLayout host_step_layout(int B, int H, int S, int d, int dtype) {
+    const size_t rows = (size_t)B * H * S;
+    const size_t elt = dtype == FA_BF16 ? 2 : 4;
+    HostStepLayout L;
+    L.arr = align_up(rows * d * elt, 256);
+    L.lse = align_up(rows * sizeof(float), 256);
+    L.ws = align_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
+    L.total = 8 * L.arr + L.lse + L.ws;
+    return L;
+}
+
 }  // namespace
 
 int fa::set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
@@ -220,6 +259,88 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     e = timed(PROF_CONV, a.stream, [&] { return fa::launch_dq_convert(a); });
     if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
     return FA_OK;
+}
+
+size_t fa_fwd_bwd_host_buffer_size(int B, int H, int S, int d, int dtype) {
+    if (B <= 0 || H <= 0 || S <= 0 || !supported_d(d) || (dtype != FA_BF16 && dtype != FA_FP32))
+        return 0;
+    return host_step_layout(B, H, S, d, dtype).total;
+}
+
+int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                    void* o, float* lse, void* dq, void* dk, void* dv,
+                    void* dev_buf, size_t dev_buf_bytes,
+                    int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(B, H, S, d, scale, dtype);
+    if (rc == 1) return FA_OK;
+    if (rc) return rc;
+    const void* in[4] = {q, k, v, dO};
+    void* out[5] = {o, lse, dq, dk, dv};
+    const char* in_name[4] = {"q", "k", "v", "dO"};
+    const char* out_name[5] = {"o", "lse", "dq", "dk", "dv"};
+    for (int i = 0; i < 4; ++i)
+        if (!in[i]) return fail(FA_ERR_INVALID_ARG, "%s is null", in_name[i]);
+    for (int i = 0; i < 5; ++i)
+        if (!out[i]) return fail(FA_ERR_INVALID_ARG, "%s is null", out_name[i]);
+    const HostStepLayout L = host_step_layout(B, H, S, d, dtype);
+    if (!dev_buf || dev_buf_bytes < L.total)
+        return fail(FA_ERR_WORKSPACE, "device buffer %p of %zu bytes, need %zu", dev_buf, dev_buf_bytes, L.total);
+    if (reinterpret_cast<uintptr_t>(dev_buf) & 255u)
+        return fail(FA_ERR_MISALIGNED, "device buffer is not 256-byte aligned");
+    const size_t rows = (size_t)B * H * S;
+    const size_t bytes = rows * d * (dtype == FA_BF16 ? 2 : 4);
+    char* base = static_cast<char*>(dev_buf);
+    void* dev[8];
+    for (int i = 0; i < 8; ++i) dev[i] = base + i * L.arr;          // q, k, v, dO, o, dq, dk, dv
+    float* lse_d = reinterpret_cast<float*>(base + 8 * L.arr);
+    void* ws = base + 8 * L.arr + L.lse;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t side = nullptr;
+    if ((rc = side_stream(stream, &side))) return rc;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};             // call start, dO copied, o/lse copied
+    for (int i = 0; i < 3; ++i) {
+        cudaError_t e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
+    }
+    cudaEvent_t ev_fwd = nullptr;
+    cudaError_t e = cudaEventCreateWithFlags(&ev_fwd, cudaEventDisableTiming);
+    auto done = [&](int r) {
+        for (int i = 0; i < 3; ++i) cudaEventDestroy(ev[i]);   // released once they have completed
+        if (ev_fwd) cudaEventDestroy(ev_fwd);
+        return r;
+    };
+    if (e != cudaSuccess) return done(cuda_fail(e, "cudaEventCreateWithFlags"));
+    // Inputs: q, k, v on the caller's stream; dO on the helper stream, after
+    // the caller's earlier work on the buffer.
+    e = cudaEventRecord(ev[0], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev[0], 0);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaMemcpyAsync(dev[i], in[i], bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dev[3], dO, bytes, cudaMemcpyHostToDevice, side);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], side);
+    if (e != cudaSuccess) return done(cuda_fail(e, "host-to-device copies"));
+    if ((rc = fa_fwd(dev[0], dev[1], dev[2], dev[4], lse_d, B, H, S, d, causal, scale, dtype, stream))) return done(rc);
+    // O and L go back on the helper stream while the backward runs.
+    e = cudaEventRecord(ev_fwd, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev_fwd, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(o, dev[4], bytes, cudaMemcpyDeviceToHost, side);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(lse, lse_d, rows * sizeof(float), cudaMemcpyDeviceToHost, side);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2], side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[1], 0);
+    if (e != cudaSuccess) return done(cuda_fail(e, "forward output copies"));
+    if ((rc = fa_bwd(dev[0], dev[1], dev[2], dev[4], dev[3], lse_d, dev[5], dev[6], dev[7], ws, L.ws,
+                     B, H, S, d, causal, scale, dtype, stream)))
+        return done(rc);
+    void* host_out[3] = {dq, dk, dv};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaMemcpyAsync(host_out[i], dev[5 + i], bytes, cudaMemcpyDeviceToHost, st);
+    // The call is complete on the caller's stream once the helper's copies are.
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2], 0);
+    if (e != cudaSuccess) return done(cuda_fail(e, "gradient copies"));
+    return done(FA_OK);
 }
 
 int fa_check_status(void* stream) {

@@ -136,6 +136,37 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 /* Size in bytes of the built-in scratch used by fa_bwd_noalloc. */
 size_t fa_bwd_noalloc_scratch_bytes(void);
 
+/*
+ * One training step of attention on HOST buffers: copy q, k, v, dO to the
+ * device, run fa_fwd and fa_bwd there, copy o, lse, dq, dk, dv back.  The
+ * pages describe no counterpart; it is the end-to-end path for callers whose
+ * tensors live in host memory (and the one the benchmark's end-to-end figure
+ * goes through).
+ *   q, k, v, dO         HOST [B,H,S,d] dtype, read only.
+ *   o, dq, dk, dv       HOST [B,H,S,d] dtype, lse HOST [B,H,S] fp32, overwritten.
+ *                       Pinned (page-locked) host memory makes every copy
+ *                       asynchronous; pageable memory works but the copies
+ *                       then synchronise with the host.
+ *   dev_buf             DEVICE buffer of >= fa_fwd_bwd_host_buffer_size()
+ *                       bytes, 256-byte aligned, owned by the caller; it holds
+ *                       device copies of all nine arrays and the backward
+ *                       workspace (q, k, v, dO, o, dq, dk, dv, lse, workspace,
+ *                       each on a 256-byte boundary).
+ * All work is ordered on `stream`: the call returns after enqueueing, and the
+ * outputs are valid once `stream` has reached the point of the call.  o and
+ * lse are copied back on a helper stream (one per caller stream, created on
+ * first use) while the backward runs, and dO is copied in on it while the
+ * forward runs; the call's work on `stream` waits for both.  Consecutive
+ * calls on different streams with different dev_buf overlap their copies and
+ * kernels.  Same size, dtype and error conventions as fa_fwd / fa_bwd;
+ * FA_ERR_WORKSPACE when dev_buf is null or too small.
+ */
+size_t fa_fwd_bwd_host_buffer_size(int B, int H, int S, int d, int dtype);
+int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
+                    void* o, float* lse, void* dq, void* dk, void* dv,
+                    void* dev_buf, size_t dev_buf_bytes,
+                    int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
 /* Message for the calling thread's last non-zero return ("" if none). */
 const char* fa_get_last_error(void);
 

@@ -81,3 +81,18 @@ def test_bwd_workspace_errors_need_no_gpu(lib):
     rc = fa.fa_bwd(P, P, P, P, P, P, P, P, P, ctypes.c_void_p(A + 16), 1 << 30, 1, 1, 128, 64, 1,
                    0.125, 0, None)
     assert rc == -3
+
+
+def test_host_step_buffer_size_and_errors_need_no_gpu(lib):
+    B, H, S, d = 2, 3, 100, 64
+    rows = B * H * S
+    up = lambda x: (x + 255) // 256 * 256
+    want = 8 * up(rows * d * 2) + up(rows * 4) + fa.bwd_workspace_size(B, H, S, d, fa.FA_BF16)
+    assert fa.fwd_bwd_host_buffer_size(B, H, S, d, fa.FA_BF16) == want
+    assert fa.fwd_bwd_host_buffer_size(B, H, S, 48, fa.FA_BF16) == 0
+    P = ctypes.c_void_p(A)
+    call = lambda buf, nbytes, **kw: lib.fa_fwd_bwd_host(
+        P, P, P, kw.get("dO", P), P, P, P, P, P, buf, nbytes, B, H, S, d, 1, 0.125, fa.FA_BF16, None)
+    assert call(ctypes.c_void_p(A), 16) == -4 and b"device buffer" in lib.fa_get_last_error()
+    assert call(ctypes.c_void_p(A + 16), 1 << 30) == -3
+    assert call(ctypes.c_void_p(A), 1 << 30, dO=ctypes.c_void_p(0)) == -1

@@ -128,6 +128,15 @@ def test_short_and_boundary_lengths(S):
     check_heads(q, k, v, do, False, 0.125, "fp32", all_heads(1, 1))
 
 
+@pytest.mark.parametrize("S", [512, 640, 896, 1152])
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_tile_pairings(S, d):
+    # Few heads: the forward runs its heaviest query tiles alone and pairs the
+    # light ones (odd and even tile counts, ragged and whole last tiles).
+    q, k, v, do = make_inputs(1, 2, S, d, "bf16", seed=7900 + S + d)
+    check_heads(q, k, v, do, True, 1.0 / math.sqrt(d), "bf16", all_heads(1, 2))
+
+
 def test_single_key_closed_form():
     q, k, v, do = make_inputs(2, 4, 1, 128, "bf16", seed=7300)
     o, lse, dq, dk, dv, _ = run_gpu(q, k, v, do, True, 0.1)
@@ -214,3 +223,52 @@ def test_device_errors_are_reported_not_raised_on_device():
         fa.fwd(bad, x, x, True)
     assert e.value.code == -3
     fa.check_status()
+
+
+# ------------------------------------------------------------------ host-buffer step
+def _host_step(q, k, v, do, causal, scale, stream=None):
+    B, H, S, d = q.shape
+    hq, hk, hv, hdo = (t.contiguous().pin_memory() for t in (q, k, v, do))
+    outs = (torch.empty_like(hq).pin_memory(), torch.empty((B, H, S), dtype=torch.float32).pin_memory(),
+            torch.empty_like(hq).pin_memory(), torch.empty_like(hq).pin_memory(), torch.empty_like(hq).pin_memory())
+    buf = torch.empty(fa.fwd_bwd_host_buffer_size(B, H, S, d, q.dtype), device=DEV, dtype=torch.uint8)
+    fa.fwd_bwd_host(hq, hk, hv, hdo, outs, buf, causal, scale, stream=stream)
+    return outs, buf
+
+
+@pytest.mark.parametrize("dtype,S,d,causal", [("bf16", 333, 64, True), ("fp32", 200, 32, False),
+                                              ("bf16", 1024, 128, True), ("bf16", 640, 80, False)])
+def test_host_buffer_step_matches_device_path_and_oracle(dtype, S, d, causal):
+    """fa_fwd_bwd_host (host in, host out) gives the device path's results
+    (the same kernels: O, L, dK, dV bit for bit, dQ up to its atomics) and
+    the oracle's."""
+    q, k, v, do = make_inputs(2, 2, S, d, dtype, seed=8100 + S + d)
+    scale = 1.0 / math.sqrt(d)
+    outs, _ = _host_step(q, k, v, do, causal, scale)
+    torch.cuda.synchronize()
+    fa.check_status()
+    o, lse, dq, dk, dv = outs
+    ref = run_gpu(q, k, v, do, causal, scale)
+    for name, a, b in (("o", o, ref[0]), ("lse", lse, ref[1]), ("dk", dk, ref[3]), ("dv", dv, ref[4])):
+        assert torch.equal(a, b), name
+    assert_close("dq vs device path", dq, ref[2], *TOL[dtype]["grad"])
+    tol = TOL[dtype]
+    for (b, h) in [(0, 0), (1, 1)]:
+        r = oracle_head(q, k, v, do, b, h, causal, scale, dtype)
+        assert_close("O", o[b, h], r["O"], *tol["o"])
+        assert_close("L", lse[b, h], r["L"], *tol["lse"])
+        for name, g in (("dQ", dq), ("dK", dk), ("dV", dv)):
+            assert_close(name, g[b, h], r[name.lower()], *tol["grad"])
+
+
+def test_host_buffer_steps_on_concurrent_streams():
+    """Steps on different streams with their own buffers overlap and stay correct."""
+    cases = [make_inputs(1, 4, 512, 64, "bf16", seed=8200 + i) for i in range(3)]
+    streams = [torch.cuda.Stream(device=DEV) for _ in cases]
+    runs = [_host_step(*c, True, 0.125, stream=st) for c, st in zip(cases, streams)]
+    torch.cuda.synchronize()
+    fa.check_status()
+    for (q, k, v, do), (outs, _) in zip(cases, runs):
+        ref = run_gpu(q, k, v, do, True, 0.125)
+        assert torch.equal(outs[0], ref[0]) and torch.equal(outs[3], ref[3]) and torch.equal(outs[4], ref[4])
+        assert_close("dq", outs[2], ref[2], *TOL["bf16"]["grad"])
