@@ -72,7 +72,7 @@ struct BwdTm {
 
 template <int D>
 struct BwdCfg {
-    static constexpr int TILE = 128 * D * 2;
+    static constexpr int TILE = Chunks<D>::tile_bytes(128);
     static constexpr int DS_BYTES = BK * BQ * 2;
     static constexpr int NDS = BwdTm<D>::PIPE ? 2 : 1;      // dS^T buffers
     static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
@@ -149,10 +149,10 @@ template <int D, bool A_TMEM>
 __device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint64_t a_desc, uint32_t b_lo, int ks,
                                            uint32_t a_mn, uint32_t acc) {
     using C = Chunks<D>;
-    if constexpr (D == 128) {
+    if constexpr (C::SINGLE_N) {
         const uint64_t bdesc = desc_make(b_lo + ks * 128, desc_hi(1024, SW_128B));
-        if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, 128, 0, 1), acc);
-        else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, 128, a_mn, 1), acc);
+        if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, D, 0, 1), acc);
+        else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, D, a_mn, 1), acc);
     } else {
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
@@ -616,7 +616,8 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     for (int i = 0; i < 4; ++i) {
         cudaError_t e;
         if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, 128)) != cudaSuccess) return e;
-        if (C::REM > 0 && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess) return e;
+        if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess)
+            return e;
     }
     {
         using QC = DqChunks<D>;

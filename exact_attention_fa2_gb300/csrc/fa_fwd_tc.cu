@@ -66,7 +66,7 @@ struct FwdTm {
 
 template <int D>
 struct FwdCfg {
-    static constexpr int TILE = BM * D * 2;
+    static constexpr int TILE = Chunks<D>::tile_bytes(BM);
     static constexpr int NS_RAW = (222 * 1024 - 2 * TILE) / (2 * TILE);
     static constexpr int NS = NS_RAW > 4 ? 4 : NS_RAW;
     static constexpr int QA_OFF = 0;
@@ -264,9 +264,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             for (int ks = 0; ks < BN / 16; ++ks) {
                 const uint32_t a_tm = tmem + TM::pcol(x) + ks * 8;
                 const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-                if constexpr (D == 128) {
+                if constexpr (C::SINGLE_N) {
                     mma_ts(tmem + TM::o(x), a_tm, desc_make(vlo + ks * 128, desc_hi(1024, SW_128B)),
-                           idesc_bf16(BM, 128, 0, 1), acc);
+                           idesc_bf16(BM, D, 0, 1), acc);
                 } else {
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c) {
@@ -503,7 +503,8 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
     for (int i = 0; i < 3; ++i) {
         cudaError_t e;
         if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, BM)) != cudaSuccess) return e;
-        if (C::REM > 0 && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, BM)) != cudaSuccess) return e;
+        if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, BM)) != cudaSuccess)
+            return e;
     }
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.lse = a.lse;
