@@ -272,3 +272,25 @@ def test_host_buffer_steps_on_concurrent_streams():
         ref = run_gpu(q, k, v, do, True, 0.125)
         assert torch.equal(outs[0], ref[0]) and torch.equal(outs[3], ref[3]) and torch.equal(outs[4], ref[4])
         assert_close("dq", outs[2], ref[2], *TOL["bf16"]["grad"])
+
+
+def test_kernels_see_the_writes_of_earlier_kernels_on_the_stream():
+    """Every kernel is launched as a programmatic dependent of the one before
+    it; an in-place PyTorch kernel right before each call must still be seen
+    (x2 and x0.5 are exact in bf16)."""
+    q, k, v, do = make_inputs(1, 2, 512, 64, "bf16", seed=8300)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    ws = torch.empty(fa.bwd_workspace_size(1, 2, 512, 64, qd.dtype), device=DEV, dtype=torch.uint8)
+    for _ in range(3):
+        qd.mul_(2)
+        o, lse = fa.fwd(qd, kd, vd, True, 0.125)
+        dod.mul_(0.5)
+        dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, True, 0.125, workspace=ws)
+    fa.check_status()
+    q8, do8 = q * 8, do * 0.125
+    for b, h in all_heads(1, 2):
+        r = oracle_head(q8, k, v, do8, b, h, True, 0.125, "bf16")
+        assert_close("O", o[b, h].cpu(), r["O"], *TOL["bf16"]["o"])
+        assert_close("dQ", dq[b, h].cpu(), r["dq"], *TOL["bf16"]["grad"])
+        assert_close("dK", dk[b, h].cpu(), r["dk"], *TOL["bf16"]["grad"])
+        assert_close("dV", dv[b, h].cpu(), r["dv"], *TOL["bf16"]["grad"])
