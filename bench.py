@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--memory", action="store_true",
+                    help="instead of timing: peak device memory of fwd+bwd against a materialised-score "
+                         "PyTorch baseline on --workload (one JSON line)")
     return ap.parse_args()
 
 
@@ -367,6 +370,10 @@ def run_ours(args, world, rank, local):
     per = lambda k: (prof[k][0] / max(prof[k][1], 1)) if prof[k][1] else None
     fwd_ms, bwd_ms = per("fwd"), per("bwd_main")
     total_kernel_ms = sum(v[0] for v in prof.values())
+    rows_all = w.B * w.H * w.S
+    elt = 2 if w.dtype == "bf16" else 4
+    pre_bytes = rows_all * (2 * w.d * elt + 4 + 4 * w.d)      # read O, dO; write D; zero dQacc
+    conv_bytes = rows_all * w.d * (4 + elt)                    # read dQacc; write dq
 
     line = {
         "metric": "attention fwd+bwd TFLOP/s (bf16, causal)",
@@ -381,6 +388,10 @@ def run_ours(args, world, rank, local):
                          "sustained": value / peaks["bf16_tflops_sustained"], "peaks": peaks["source"]},
         "kernels": {"fwd_ms": fwd_ms, "bwd_main_ms": bwd_ms,
                     "bwd_preprocess_ms": per("bwd_preprocess"), "dq_convert_ms": per("dq_convert"),
+                    # HBM-bound helpers: algorithmic bytes over time against the measured copy rate.
+                    "bwd_preprocess_gbs": (pre_bytes / (per("bwd_preprocess") * 1e-3) / 1e9) if per("bwd_preprocess") else None,
+                    "dq_convert_gbs": (conv_bytes / (per("dq_convert") * 1e-3) / 1e9) if per("dq_convert") else None,
+                    "hbm_peak_gbs": peaks["hbm_gbs"],
                     "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
                     "bwd_tflops": 2.5 * f_fwd / ((ms_per_step - fwd_ms) * 1e-3) / 1e12 if fwd_ms else None,
                     "shares": {k: (v[0] / total_kernel_ms if total_kernel_ms else None) for k, v in prof.items()}},
@@ -402,12 +413,58 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def peak_memory_bytes(fn):
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    fn()
+    torch.cuda.synchronize()
+    return torch.cuda.max_memory_allocated() - base
+
+
+def run_memory(args):
+    """Peak device memory above the inputs of one fwd+bwd step: this library
+    against the materialised computation (QK^T -> masked softmax -> PV in the
+    storage dtype, PyTorch autograd), which holds S x S score tensors."""
+    import exact_attention_fa2_gb300 as fa
+    dev = torch.device("cuda", 0)
+    fa.load_library()
+    w = workload(args.workload)
+    q, k, v, do = (t.to(dev) for t in make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed, w.qkv_scale))
+
+    def ours():
+        o, lse = fa.fwd(q, k, v, True, w.scale)
+        fa.bwd(q, k, v, o, do, lse, True, w.scale)
+
+    def materialised():
+        qq, kk, vv = (t.detach().requires_grad_() for t in (q, k, v))
+        s_ = torch.matmul(qq, kk.transpose(-1, -2)) * w.scale
+        mask = torch.ones(w.S, w.S, device=dev, dtype=torch.bool).triu(1)
+        p_ = torch.softmax(s_.masked_fill(mask, float("-inf")), dim=-1)
+        out = torch.matmul(p_, vv)
+        out.backward(do)
+
+    ours()
+    fa.check_status()
+    m_ours = peak_memory_bytes(ours)
+    fa.check_status()
+    m_mat = peak_memory_bytes(materialised)
+    line = {"memory": {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
+                       "ours_peak_bytes": m_ours, "materialised_peak_bytes": m_mat,
+                       "ratio": m_mat / max(m_ours, 1),
+                       "what": "torch.cuda.max_memory_allocated above the resident inputs, one fwd+bwd"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.memory:
+            return run_memory(args)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -294,3 +294,26 @@ def test_kernels_see_the_writes_of_earlier_kernels_on_the_stream():
         assert_close("dQ", dq[b, h].cpu(), r["dq"], *TOL["bf16"]["grad"])
         assert_close("dK", dk[b, h].cpu(), r["dk"], *TOL["bf16"]["grad"])
         assert_close("dV", dv[b, h].cpu(), r["dv"], *TOL["bf16"]["grad"])
+
+
+def test_peak_memory_far_below_materialised():
+    """The score matrix is never written: fwd+bwd needs O(S*d) device memory
+    (outputs and the fp32 workspace) where the materialised computation holds
+    S x S score tensors."""
+    B, H, S, d = 1, 16, 2048, 64
+    q, k, v, do = (t.to(DEV) for t in make_inputs(B, H, S, d, "bf16", seed=8400))
+    o, lse = fa.fwd(q, k, v, True)
+    fa.bwd(q, k, v, o, do, lse, True)
+    del o, lse
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    o, lse = fa.fwd(q, k, v, True)
+    fa.bwd(q, k, v, o, do, lse, True)
+    torch.cuda.synchronize()
+    ours = torch.cuda.max_memory_allocated() - base
+    fa.check_status()
+    elt_bytes = B * H * S * d * 2
+    # o, dq, dk, dv (bf16), lse, and the fp32 workspace (D + dQacc): about 6.1x one input.
+    assert ours <= 7 * elt_bytes, ours
+    assert ours * 4 < B * H * S * S * 2          # under a quarter of ONE bf16 S x S score tensor
