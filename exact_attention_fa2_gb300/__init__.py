@@ -82,6 +82,10 @@ def load_library():
         lib.fa_profile_enable.restype = i
         lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
         lib.fa_profile_read.restype = i
+        lib.fa_fwd_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_partial.restype = i
+        lib.fa_merge.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_merge.restype = i
         lib.fa_fwd_bwd_host_buffer_size.argtypes = [i, i, i, i, i]
         lib.fa_fwd_bwd_host_buffer_size.restype = sz
         lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
@@ -202,6 +206,45 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
                     B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
     _check(rc)
     return dq, dk, dv
+
+
+def fwd_partial(q, k, v, key_begin: int, key_end: int, causal: bool = False, scale=None, out=None, stream=None):
+    """Attention of every query over keys [key_begin, key_end) only (causal
+    positions are whole-sequence positions); returns (o_part fp32, lse_part
+    fp32), with o = 0 and lse = -inf where a query has no admissible key."""
+    _check_qkv(q, k, v)
+    B, H, S, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        o = torch.empty((B, H, S, d), device=q.device, dtype=torch.float32)
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    else:
+        o, lse = out
+    with torch.cuda.device(q.device):
+        rc = load_library().fa_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, d,
+                                           int(key_begin), int(key_end), int(causal), scale, _dtype_code(q),
+                                           ctypes.c_void_p(_stream_handle(stream)))
+    _check(rc)
+    return o, lse
+
+
+def merge(o_a, lse_a, o_b, lse_b, dtype=torch.bfloat16, out=None, stream=None):
+    """Exact merge of two partial results over disjoint key sets: returns
+    (o in ``dtype``, lse fp32)."""
+    B, H, S, d = o_a.shape
+    for t in (o_a, o_b):
+        if t.dtype != torch.float32 or t.shape != o_a.shape or not t.is_contiguous():
+            raise ValueError("partial outputs must be contiguous fp32 [B, H, S, d] tensors")
+    if out is None:
+        o = torch.empty((B, H, S, d), device=o_a.device, dtype=dtype)
+        lse = torch.empty((B, H, S), device=o_a.device, dtype=torch.float32)
+    else:
+        o, lse = out
+    with torch.cuda.device(o_a.device):
+        rc = load_library().fa_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse),
+                                     B, H, S, d, _dtype_code(o), ctypes.c_void_p(_stream_handle(stream)))
+    _check(rc)
+    return o, lse
 
 
 def fwd_bwd_host_buffer_size(B: int, H: int, S: int, d: int, dtype) -> int:

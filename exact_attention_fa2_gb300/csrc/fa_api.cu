@@ -220,6 +220,46 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     return FA_OK;
 }
 
+int fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                   int B, int H, int S, int d, int key_begin, int key_end, int causal, float scale, int dtype,
+                   void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(B, H, S, d, scale, dtype);
+    if (rc == 1) return FA_OK;
+    if (rc) return rc;
+    if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+        (rc = check_ptr(o_part, "o_part")) || (rc = check_ptr(lse_part, "lse_part")))
+        return rc;
+    if (key_begin < 0 || key_end > S || key_begin >= key_end)
+        return fail(FA_ERR_INVALID_ARG, "key window [%d, %d) is empty or outside [0, %d)", key_begin, key_end, S);
+    if (key_begin % 128 != 0)
+        return fail(FA_ERR_UNSUPPORTED, "key_begin %d is not a multiple of 128", key_begin);
+    fa::FwdArgs a{q, k, v, nullptr, lse_part, B, H, S, d, causal ? 1 : 0, scale, dtype,
+                  static_cast<cudaStream_t>(stream), nullptr};
+    if ((rc = status_ptr(&a.status))) return rc;
+    cudaError_t e = timed(PROF_FWD, a.stream, [&] {
+        return dtype == FA_BF16 ? fa::launch_fwd_tc_partial(a, key_begin, key_end, o_part)
+                                : fa::launch_fwd_simt_partial(a, key_begin, key_end, o_part);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "partial forward launch");
+    return FA_OK;
+}
+
+int fa_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, void* o, float* lse,
+             int B, int H, int S, int d, int dtype, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(B, H, S, d, 1.f, dtype);
+    if (rc == 1) return FA_OK;
+    if (rc) return rc;
+    if ((rc = check_ptr(o_a, "o_a")) || (rc = check_ptr(lse_a, "lse_a")) || (rc = check_ptr(o_b, "o_b")) ||
+        (rc = check_ptr(lse_b, "lse_b")) || (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")))
+        return rc;
+    fa::MergeArgs a{o_a, lse_a, o_b, lse_b, o, lse, (long long)B * H * S, d, dtype, static_cast<cudaStream_t>(stream)};
+    cudaError_t e = fa::launch_merge(a);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return FA_OK;
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype) {
     if (B <= 0 || H <= 0 || S <= 0 || !supported_d(d) || (dtype != FA_BF16 && dtype != FA_FP32))
         return 0;

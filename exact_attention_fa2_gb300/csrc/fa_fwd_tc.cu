@@ -89,11 +89,14 @@ struct FwdParams {
     CUtensorMap tk[2];
     CUtensorMap tv[2];
     __nv_bfloat16* o;
+    float* o32;       // partial attention: fp32 output (o unused)
     float* lse;
     unsigned int* status;
-    int S;
+    int S;            // query rows (and the row pitch of every array)
     int n_units;      // 256-row query blocks per head
-    int n_kv;
+    int Sk;           // key rows seen by the K/V tensor maps
+    int n_kv;         // 128-key tiles in [0, Sk)
+    int dshift;       // causal: key tile j is on query tile t's diagonal when j = t + dshift (<= 0)
     int causal;
     float c;          // |scale| * log2(e), at least 1e-30
     uint32_t neg_a;   // 1 when scale < 0: the S product negates Q
@@ -114,7 +117,12 @@ __device__ __forceinline__ void exp_pairs(const uint32_t* r, uint64_t c2, uint64
     }
 }
 
-template <int D>
+// PARTIAL: attention of every query over the key window the K/V tensor maps
+// start at (keys k0 + [0, Sk)), causal positions shifted by dshift tiles
+// (k0 = -128 dshift); O is written normalised in fp32 and a query tile with
+// no admissible key gets O = 0, L = -inf.  This is one side of the split-KV
+// merge (see fa_merge_kernel).
+template <int D, bool PARTIAL>
 __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_constant__ FwdParams p) {
     using C = Chunks<D>;
     using G = FwdCfg<D>;
@@ -149,9 +157,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     const int S = p.S;
     const int qtA = 2 * unit;
     const bool hasB = (qtA + 1) * BM < S;
-    // Last key tile of each query tile (inclusive); jB >= jA.
-    const int jA = p.causal ? min(qtA, p.n_kv - 1) : p.n_kv - 1;
-    const int jB = hasB ? (p.causal ? min(qtA + 1, p.n_kv - 1) : p.n_kv - 1) : jA;
+    // Last key tile of each query tile (inclusive, -1: none); jB >= jA.
+    const int jA = p.causal ? min(qtA + p.dshift, p.n_kv - 1) : p.n_kv - 1;
+    const int jB = hasB ? (p.causal ? min(qtA + 1 + p.dshift, p.n_kv - 1) : p.n_kv - 1) : jA;
+    const int n_issuers = TM::PSEP ? (jA >= 0 ? 1 : 0) + ((hasB && jB >= 0) ? 1 : 0) : 1;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -160,9 +169,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         // alone, is never refilled).
         for (int s = 0; s < NS; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), (TM::PSEP && hasB) ? 2 : 1);
+            mbar_init(k_empty(s), n_issuers > 0 ? n_issuers : 1);
             mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), (TM::PSEP && hasB) ? 2 : 1);
+            mbar_init(v_empty(s), n_issuers > 0 ? n_issuers : 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(s_full(x), 1);
@@ -279,13 +288,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             }
             mma_commit(o_done(x));
         };
-        bool ok = warp_wait(q_full, 0, abort, p.status);
+        // Nothing to multiply when no key tile is admissible (partial attention).
+        bool ok = jB >= 0 && warp_wait(q_full, 0, abort, p.status);
         if (ok) ok = warp_wait(k_full(0), 0, abort, p.status);
         if constexpr (TM::PSEP) {
             // One issuer per tile; the next scores go in as soon as the
             // softmax has read these.
             const int x = warp - MMA_WARP;
             const int jX = x ? jB : jA;
+            if (jX < 0) ok = false;
             if (ok) {
                 tc_fence_after();
                 if (lane == 0) {
@@ -323,8 +334,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             if (ok) {
                 tc_fence_after();
                 if (lane == 0) {
-                    issue_s(0, 0);
-                    if (hasB) issue_s(1, 0);
+                    if (tile_has(0, 0)) issue_s(0, 0);
+                    if (tile_has(1, 0)) issue_s(1, 0);
                     mma_commit(k_empty(0));
                 }
                 __syncwarp();
@@ -374,7 +385,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
         const uint32_t tP = tmem + lane_off + TM::pcol(x);
         const uint32_t tO = tmem + lane_off + TM::o(x);
         const float c = p.c;
-        const int key_lim = p.causal ? min(row, S - 1) : S - 1;
+        const int Sk = p.Sk;
+        const int key_lim = p.causal ? min(row + BM * p.dshift, Sk - 1) : Sk - 1;   // in window coordinates
         float m_use = -INFINITY;
         float l_sum = 0.f;
         bool ok = true;
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             // Only the diagonal tile of a causal row block and a ragged last
             // tile need the per-element mask; masked scores become -inf.
             const int kbase = j * BN;
-            const bool masked = (p.causal && j == qt) || (kbase + BN > S);
+            const bool masked = (p.causal && j == qt + p.dshift) || (kbase + BN > Sk);
             if (masked) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i)
@@ -461,22 +473,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             mbar_arrive(p_full(x));
         }
         // Epilogue (Algorithm 1 lines 15-18): O / l and L = (m + log2 l) ln 2.
-        if (ok && warp_wait(o_done(x), jX & 1, abort, p.status)) {
+        if (ok && jX < 0) {
+            // No admissible key in the window (partial attention only).
+            if constexpr (PARTIAL) {
+                if (row < S) {
+                    float4* dst = reinterpret_cast<float4*>(p.o32 + ((size_t)bh * S + row) * D);
+#pragma unroll
+                    for (int u = 0; u < D / 4; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    p.lse[(size_t)bh * S + row] = -INFINITY;
+                }
+            }
+        } else if (ok && warp_wait(o_done(x), jX & 1, abort, p.status)) {
             tc_fence_after();
             const float inv = 1.f / l_sum;
-            __nv_bfloat16* orow = p.o + ((size_t)bh * S + row) * D;
 #pragma unroll
             for (int u = 0; u < D / 16; ++u) {
                 uint32_t o[16];
                 tmem_ld16(tO + 16 * u, o);
                 tmem_wait_ld();
                 reg_fence<16>(o);
-                uint32_t pk[8];
+                if (row >= S) continue;
+                if constexpr (PARTIAL) {
+                    float4* dst = reinterpret_cast<float4*>(p.o32 + ((size_t)bh * S + row) * D + 16 * u);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                if (row < S) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 16 * u);
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                } else {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * S + row) * D + 16 * u);
                     dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
@@ -491,32 +519,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D>
-cudaError_t fwd_tc_launch(const FwdArgs& a) {
+template <int D, bool PARTIAL>
+cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o32) {
     using C = Chunks<D>;
     using G = FwdCfg<D>;
     FwdParams p;
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
-    const void* src[3] = {a.q, a.k, a.v};
+    // K and V tensor maps start at the key window; rows keep the pitch of S.
+    const int Sk = key_end - key_begin;
+    const size_t koff = (size_t)key_begin * D * 2;
+    const void* src[3] = {a.q, static_cast<const char*>(a.k) + koff, static_cast<const char*>(a.v) + koff};
+    const int rows[3] = {a.S, Sk, Sk};
     CUtensorMap* maps[3] = {p.tq, p.tk, p.tv};
     for (int i = 0; i < 3; ++i) {
         cudaError_t e;
-        if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, BM)) != cudaSuccess) return e;
-        if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, BM)) != cudaSuccess)
+        if (C::N64 > 0 && (e = make_tmap_bf16_3d_rows(&maps[i][0], src[i], D, rows[i], a.S, BH, 64, BM)) != cudaSuccess)
+            return e;
+        if (C::REM > 0 && !C::PAD &&
+            (e = make_tmap_bf16_3d_rows(&maps[i][1], src[i], D, rows[i], a.S, BH, C::REM, BM)) != cudaSuccess)
             return e;
     }
     p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.o32 = o32;
     p.lse = a.lse;
     p.status = a.status;
     p.S = a.S;
     p.n_units = (a.S + 2 * BM - 1) / (2 * BM);
-    p.n_kv = (a.S + BN - 1) / BN;
+    p.Sk = Sk;
+    p.n_kv = (Sk + BN - 1) / BN;
+    p.dshift = -(key_begin / BN);
     p.causal = a.causal;
     float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;
     p.neg_a = a.scale < 0.f ? 1u : 0u;
-    auto kern = fwd_tc_kernel<D>;
+    auto kern = fwd_tc_kernel<D, PARTIAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_units * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
@@ -526,12 +563,24 @@ cudaError_t fwd_tc_launch(const FwdArgs& a) {
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
     switch (a.d) {
-        case 16: return fwd_tc_launch<16>(a);
-        case 32: return fwd_tc_launch<32>(a);
-        case 64: return fwd_tc_launch<64>(a);
-        case 80: return fwd_tc_launch<80>(a);
-        case 96: return fwd_tc_launch<96>(a);
-        case 128: return fwd_tc_launch<128>(a);
+        case 16: return fwd_tc_launch<16, false>(a, 0, a.S, nullptr);
+        case 32: return fwd_tc_launch<32, false>(a, 0, a.S, nullptr);
+        case 64: return fwd_tc_launch<64, false>(a, 0, a.S, nullptr);
+        case 80: return fwd_tc_launch<80, false>(a, 0, a.S, nullptr);
+        case 96: return fwd_tc_launch<96, false>(a, 0, a.S, nullptr);
+        case 128: return fwd_tc_launch<128, false>(a, 0, a.S, nullptr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_fwd_tc_partial(const FwdArgs& a, int key_begin, int key_end, float* o32) {
+    switch (a.d) {
+        case 16: return fwd_tc_launch<16, true>(a, key_begin, key_end, o32);
+        case 32: return fwd_tc_launch<32, true>(a, key_begin, key_end, o32);
+        case 64: return fwd_tc_launch<64, true>(a, key_begin, key_end, o32);
+        case 80: return fwd_tc_launch<80, true>(a, key_begin, key_end, o32);
+        case 96: return fwd_tc_launch<96, true>(a, key_begin, key_end, o32);
+        case 128: return fwd_tc_launch<128, true>(a, key_begin, key_end, o32);
         default: return cudaErrorInvalidValue;
     }
 }

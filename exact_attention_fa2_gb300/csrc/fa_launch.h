@@ -78,6 +78,24 @@ int set_last_error(int code, const char* msg);
 
 // bf16 tensor-core (tcgen05) kernels.
 cudaError_t launch_fwd_tc(const FwdArgs& a);
+// Partial forward over keys [key_begin, key_end) (key_begin a multiple of
+// 128): normalised fp32 O into o32, L into a.lse (-inf where no key).
+cudaError_t launch_fwd_tc_partial(const FwdArgs& a, int key_begin, int key_end, float* o32);
+cudaError_t launch_fwd_simt_partial(const FwdArgs& a, int key_begin, int key_end, float* o32);
+// Merge of two partial results over disjoint key sets.
+struct MergeArgs {
+    const float* o_a;
+    const float* lse_a;
+    const float* o_b;
+    const float* lse_b;
+    void* o;
+    float* lse;
+    long long rows;
+    int d;
+    int dtype;
+    cudaStream_t stream;
+};
+cudaError_t launch_merge(const MergeArgs& a);
 cudaError_t launch_bwd_tc(const BwdArgs& a);
 
 }  // namespace fa

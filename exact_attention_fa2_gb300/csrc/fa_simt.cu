@@ -62,7 +62,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(NT)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 T* __restrict__ o, float* __restrict__ lse, int S, int n_qtiles, int causal,
-                float scale_log2) {
+                float scale_log2, int kb, int ke) {
+    // Keys [kb, ke) only (the whole row for the plain forward); a row with no
+    // admissible key gets O = 0 and L = -inf (partial attention).
     extern __shared__ float smem[];
     constexpr int LDQ = D + 1, LDK = D + 1, LDV = D;
     constexpr int NC = D / 16;
@@ -89,13 +91,13 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
 
-    int n_k = (S + BK - 1) / BK;
-    if (causal) n_k = min(n_k, qt + 1);   // tiles above the diagonal are fully masked
+    int n_k = (ke - kb + BK - 1) / BK;
+    if (causal) n_k = min(n_k, q0 + BQ - 1 >= kb ? (q0 + BQ - 1 - kb) / BK + 1 : 0);   // fully masked tiles skipped
 
     for (int kt = 0; kt < n_k; ++kt) {
         __syncthreads();
-        load_tile<T, D>(Ks, LDK, k + base, kt * BK, S);
-        load_tile<T, D>(Vs, LDV, v + base, kt * BK, S);
+        load_tile<T, D>(Ks, LDK, k + base, kb + kt * BK, ke);
+        load_tile<T, D>(Vs, LDV, v + base, kb + kt * BK, ke);
         __syncthreads();
 
         // S tile (Algorithm 1 line 9), rows ty*4+r, columns tx+16c.
@@ -121,8 +123,8 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
             const int row = q0 + ty * 4 + r;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int col = kt * BK + tx + 16 * c;
-                const bool keep = col < S && (!causal || col <= row);
+                const int col = kb + kt * BK + tx + 16 * c;
+                const bool keep = col < ke && (!causal || col <= row);
                 Ps[(ty * 4 + r) * LDP + tx + 16 * c] = keep ? s[r][c] * scale_log2 : -INFINITY;
             }
         }
@@ -187,14 +189,14 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
         const int lr = ty * 4 + r;
         const int row = q0 + lr;
         if (row < S) {
-            const float inv = 1.f / l_s[lr];
+            const float inv = l_s[lr] > 0.f ? 1.f / l_s[lr] : 0.f;
 #pragma unroll
             for (int c = 0; c < NC; ++c)
                 o[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(acc[r][c] * inv);
         }
     }
     if (tid < 64 && q0 + tid < S)
-        lse[(size_t)blockIdx.y * S + q0 + tid] = (m_s[tid] + log2f(l_s[tid])) * FA_LN2;
+        lse[(size_t)blockIdx.y * S + q0 + tid] = l_s[tid] > 0.f ? (m_s[tid] + log2f(l_s[tid])) * FA_LN2 : -INFINITY;
 }
 
 template <typename T, int D>
@@ -344,15 +346,15 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 }
 
 template <typename T, int D>
-cudaError_t fwd_simt_launch(const FwdArgs& a) {
+cudaError_t fwd_simt_launch(const FwdArgs& a, int kb, int ke, T* o) {
     constexpr size_t smem = fwd_smem_bytes<D>();
     auto kern = fwd_simt_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int n_qtiles = (a.S + BQ - 1) / BQ;
     dim3 grid(n_qtiles, a.B * a.H);
-    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (T*)a.o, a.lse,
-                                       a.S, n_qtiles, a.causal, a.scale * FA_LOG2E);
+    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, o, a.lse,
+                                       a.S, n_qtiles, a.causal, a.scale * FA_LOG2E, kb, ke);
     return cudaGetLastError();
 }
 
@@ -370,14 +372,14 @@ cudaError_t bwd_simt_launch(const BwdArgs& a) {
 }
 
 template <typename T>
-cudaError_t fwd_simt_dispatch(const FwdArgs& a) {
+cudaError_t fwd_simt_dispatch(const FwdArgs& a, int kb, int ke, T* o) {
     switch (a.d) {
-        case 16: return fwd_simt_launch<T, 16>(a);
-        case 32: return fwd_simt_launch<T, 32>(a);
-        case 64: return fwd_simt_launch<T, 64>(a);
-        case 80: return fwd_simt_launch<T, 80>(a);
-        case 96: return fwd_simt_launch<T, 96>(a);
-        case 128: return fwd_simt_launch<T, 128>(a);
+        case 16: return fwd_simt_launch<T, 16>(a, kb, ke, o);
+        case 32: return fwd_simt_launch<T, 32>(a, kb, ke, o);
+        case 64: return fwd_simt_launch<T, 64>(a, kb, ke, o);
+        case 80: return fwd_simt_launch<T, 80>(a, kb, ke, o);
+        case 96: return fwd_simt_launch<T, 96>(a, kb, ke, o);
+        case 128: return fwd_simt_launch<T, 128>(a, kb, ke, o);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -398,7 +400,14 @@ cudaError_t bwd_simt_dispatch(const BwdArgs& a) {
 }  // namespace
 
 cudaError_t launch_fwd_simt(const FwdArgs& a) {
-    return a.dtype == DT_FP32 ? fwd_simt_dispatch<float>(a) : fwd_simt_dispatch<__nv_bfloat16>(a);
+    return a.dtype == DT_FP32 ? fwd_simt_dispatch<float>(a, 0, a.S, (float*)a.o)
+                              : fwd_simt_dispatch<__nv_bfloat16>(a, 0, a.S, (__nv_bfloat16*)a.o);
+}
+
+cudaError_t launch_fwd_simt_partial(const FwdArgs& a, int key_begin, int key_end, float* o32) {
+    // fp32 storage only: the partial output is fp32 like the inputs.
+    if (a.dtype != DT_FP32) return cudaErrorInvalidValue;
+    return fwd_simt_dispatch<float>(a, key_begin, key_end, o32);
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a) {

@@ -32,10 +32,10 @@ cudaError_t encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 
 struct Key {
     const void* base;
-    int elt_bytes, d, S, BH, box_w, box_rows;
+    int elt_bytes, d, rows, pitch, BH, box_w, box_rows;
     bool operator==(const Key& o) const {
-        return base == o.base && elt_bytes == o.elt_bytes && d == o.d && S == o.S && BH == o.BH &&
-               box_w == o.box_w && box_rows == o.box_rows;
+        return base == o.base && elt_bytes == o.elt_bytes && d == o.d && rows == o.rows && pitch == o.pitch &&
+               BH == o.BH && box_w == o.box_w && box_rows == o.box_rows;
     }
 };
 
@@ -49,11 +49,12 @@ std::mutex g_mu;
 Entry g_cache[kCache];
 int g_next = 0;
 
-// Encode a 3-D tiled map over a contiguous [BH, S, d] array of bf16 (2-byte)
-// or fp32 (4-byte) elements; swizzle chosen from the box's inner bytes.
-cudaError_t encode_3d(CUtensorMap* map, const void* base, int elt_bytes, int d, int S, int BH, int box_w,
-                      int box_rows) {
-    const Key key{base, elt_bytes, d, S, BH, box_w, box_rows};
+// Encode a 3-D tiled map over `rows` rows of d bf16 (2-byte) or fp32 (4-byte)
+// elements per head, heads `pitch` rows apart; swizzle chosen from the box's
+// inner bytes.
+cudaError_t encode_3d(CUtensorMap* map, const void* base, int elt_bytes, int d, int rows, int pitch, int BH,
+                      int box_w, int box_rows) {
+    const Key key{base, elt_bytes, d, rows, pitch, BH, box_w, box_rows};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int i = 0; i < kCache; ++i) {
@@ -71,8 +72,8 @@ cudaError_t encode_3d(CUtensorMap* map, const void* base, int elt_bytes, int d, 
                            : inner_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                            : inner_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
                                                 : CU_TENSOR_MAP_SWIZZLE_NONE;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)d * elt_bytes, (cuuint64_t)S * d * elt_bytes};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elt_bytes, (cuuint64_t)pitch * d * elt_bytes};
     cuuint32_t box[3] = {(cuuint32_t)box_w, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -89,11 +90,16 @@ cudaError_t encode_3d(CUtensorMap* map, const void* base, int elt_bytes, int d, 
 
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w,
                               int box_rows) {
-    return encode_3d(map, base, 2, d, S, BH, box_w, box_rows);
+    return encode_3d(map, base, 2, d, S, S, BH, box_w, box_rows);
+}
+
+cudaError_t make_tmap_bf16_3d_rows(CUtensorMap* map, const void* base, int d, int rows, int pitch, int BH,
+                                   int box_w, int box_rows) {
+    return encode_3d(map, base, 2, d, rows, pitch, BH, box_w, box_rows);
 }
 
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w, int box_rows) {
-    return encode_3d(map, base, 4, d, S, BH, box_w, box_rows);
+    return encode_3d(map, base, 4, d, S, S, BH, box_w, box_rows);
 }
 
 }  // namespace fa

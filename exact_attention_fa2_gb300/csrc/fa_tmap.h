@@ -13,6 +13,11 @@ namespace fa {
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w,
                               int box_rows);
 
+// Same over the first `rows` rows of each head of a [BH, pitch, d] bf16
+// array (base may point inside the first head: a window of key rows).
+cudaError_t make_tmap_bf16_3d_rows(CUtensorMap* map, const void* base, int d, int rows, int pitch, int BH,
+                                   int box_w, int box_rows);
+
 // Same over a contiguous [BH, S, d] fp32 array (box inner extent 64 or 128
 // bytes, matching swizzle), used to reduce-add tiles into it.
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const void* base, int d, int S, int BH, int box_w, int box_rows);

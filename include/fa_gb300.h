@@ -79,6 +79,37 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * Split-KV building block ("[Attention] FlashAttention/Ring-Attention/...统一
+ * 原理": attention over a subset of the keys, merged exactly afterwards).
+ *
+ * fa_fwd_partial: every query attends only to keys [key_begin, key_end)
+ * (causal: also key <= query, in whole-sequence positions).
+ *   q, k, v      [B,H,S,d] dtype, the whole sequence, read only.
+ *   o_part       [B,H,S,d] fp32, overwritten with the output normalised over
+ *                the window's keys (0 for a query with no admissible key).
+ *   lse_part     [B,H,S] fp32, overwritten with the natural-log logsumexp of
+ *                the window's scores (-inf for a query with no admissible key).
+ *   key_begin    a multiple of 128; 0 <= key_begin < key_end <= S.
+ * Same conventions as fa_fwd otherwise (bf16 on the tensor cores, P rounded to
+ * bf16 before its product; fp32 on the FMA pipes).
+ *
+ * fa_merge: combine two partial results over disjoint key sets of the same
+ * queries: L = log(e^lse_a + e^lse_b), o = e^(lse_a - L) o_a + e^(lse_b - L) o_b.
+ *   o_a, o_b     [B,H,S,d] fp32 (fa_fwd_partial outputs, or merges of them).
+ *   lse_a, lse_b [B,H,S] fp32.
+ *   o            [B,H,S,d] dtype (bf16 rounded to nearest even, or fp32).
+ *   lse          [B,H,S] fp32.
+ * o may alias o_a (or o_b) when dtype is FA_FP32, so merges can chain; lse
+ * must not alias lse_a or lse_b.  Merging the partials of key windows that
+ * tile [0, S) gives fa_fwd's result up to rounding.
+ */
+int fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                   int B, int H, int S, int d, int key_begin, int key_end, int causal, float scale, int dtype,
+                   void* stream);
+int fa_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b, void* o, float* lse,
+             int B, int H, int S, int d, int dtype, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs.  The workspace holds, in order,
  *   D      [B,H,S] fp32   D_i = rowsum(O * dO)_i (handout, "backward pass with
  *                         recomputation"; Algorithm 2 step 2), written by fa_bwd;

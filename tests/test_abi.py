@@ -96,3 +96,16 @@ def test_host_step_buffer_size_and_errors_need_no_gpu(lib):
     assert call(ctypes.c_void_p(A), 16) == -4 and b"device buffer" in lib.fa_get_last_error()
     assert call(ctypes.c_void_p(A + 16), 1 << 30) == -3
     assert call(ctypes.c_void_p(A), 1 << 30, dO=ctypes.c_void_p(0)) == -1
+
+
+def test_partial_and_merge_argument_errors_need_no_gpu(lib):
+    P = ctypes.c_void_p(A)
+    part = lambda kb, ke, **kw: lib.fa_fwd_partial(P, P, P, P, P, 1, 2, 512, 64, kb, ke, 1, 0.125,
+                                                   kw.get("dtype", fa.FA_BF16), None)
+    assert part(64, 512) == -2 and b"multiple of 128" in lib.fa_get_last_error()
+    assert part(256, 256) == -1
+    assert part(0, 600) == -1
+    assert part(-128, 256) == -1
+    mrg = lambda **kw: lib.fa_merge(P, P, kw.get("o_b", P), P, P, P, 1, 2, 512, kw.get("d", 64), fa.FA_BF16, None)
+    assert mrg(o_b=ctypes.c_void_p(0)) == -1
+    assert mrg(d=48) == -2

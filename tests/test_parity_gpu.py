@@ -317,3 +317,68 @@ def test_peak_memory_far_below_materialised():
     # o, dq, dk, dv (bf16), lse, and the fp32 workspace (D + dQacc): about 6.1x one input.
     assert ours <= 7 * elt_bytes, ours
     assert ours * 4 < B * H * S * S * 2          # under a quarter of ONE bf16 S x S score tensor
+
+
+# ------------------------------------------------------------------ split-KV and merge
+def _oracle_partial(q, k, v, b, h, keys, causal, scale):
+    o, m, Bsum = oracle.partial_attention(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), keys, causal, scale)
+    with np.errstate(divide="ignore"):
+        L = np.where(np.isfinite(m), m + np.log(np.where(Bsum > 0, Bsum, 1.0)), -np.inf)
+    return o, L
+
+
+def _check_partial(o, lse, ref_o, ref_L, tol):
+    o, lse = f64(o), f64(lse)
+    empty = ~np.isfinite(ref_L)
+    assert np.all(np.isneginf(lse[empty])), "rows without keys must carry L = -inf"
+    assert np.all(o[empty] == 0.0), "rows without keys must carry O = 0"
+    ok = ~empty
+    assert_close("O part", o[ok], ref_o[ok], *tol["o"])
+    assert_close("L part", lse[ok], ref_L[ok], *tol["lse"])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_partial_windows_match_oracle(dtype, causal):
+    """Attention over one key window equals the oracle's partial softmax over
+    the same keys (queries before the window: O = 0, L = -inf when causal)."""
+    B, H, S, d = 1, 2, 333, 64
+    q, k, v, _ = make_inputs(B, H, S, d, dtype, seed=8500 + causal)
+    scale = 1.0 / math.sqrt(d)
+    tol = TOL[dtype]
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    for kb, ke in [(0, 128), (128, 333), (256, 300), (0, 333)]:
+        o, lse = fa.fwd_partial(qd, kd, vd, kb, ke, causal, scale)
+        fa.check_status()
+        o, lse = o.cpu(), lse.cpu()
+        for b, h in all_heads(B, H):
+            ref_o, ref_L = _oracle_partial(q, k, v, b, h, np.arange(kb, ke), causal, scale)
+            _check_partial(o[b, h], lse[b, h], ref_o, ref_L, tol)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("bf16", 80), ("fp32", 32)])
+def test_split_kv_merge_equals_full_attention(dtype, d):
+    """Partials over windows that tile the keys, merged pairwise (the chain
+    keeps fp32 in between), give the full attention: against fa_fwd and the
+    oracle's two-half merge."""
+    B, H, S = 1, 3, 640
+    q, k, v, _ = make_inputs(B, H, S, d, dtype, seed=8600 + d)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    edges = [0, 256, 384, S]
+    parts = [fa.fwd_partial(qd, kd, vd, a, b, True, scale) for a, b in zip(edges[:-1], edges[1:])]
+    o_acc, l_acc = parts[0]
+    for o_p, l_p in parts[1:-1]:
+        o_acc, l_acc = fa.merge(o_acc, l_acc, o_p, l_p, torch.float32)
+    o, lse = fa.merge(o_acc, l_acc, parts[-1][0], parts[-1][1], qd.dtype)
+    o_full, lse_full = fa.fwd(qd, kd, vd, True, scale)
+    fa.check_status()
+    tol = TOL[dtype]
+    assert_close("O merged vs fa_fwd", o.cpu(), f64(o_full.cpu()), *tol["o"])
+    assert_close("L merged vs fa_fwd", lse.cpu(), f64(lse_full.cpu()), *tol["lse"])
+    for b, h in all_heads(B, H):
+        oa, ma, Ba = oracle.partial_attention(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), np.arange(0, 256), True, scale)
+        ob, mb, Bb = oracle.partial_attention(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), np.arange(256, S), True, scale)
+        ref_o, _, _, ref_L = oracle.merge_two_halves(oa, ma, Ba, ob, mb, Bb)
+        assert_close("O merged vs oracle", o[b, h].cpu(), ref_o, *tol["o"])
+        assert_close("L merged vs oracle", lse[b, h].cpu(), ref_L, *tol["lse"])
