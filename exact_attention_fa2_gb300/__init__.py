@@ -23,7 +23,7 @@ import threading
 import torch
 
 __all__ = [
-    "FAError", "library_path", "load_library", "fa_fwd", "fa_bwd", "fwd", "bwd",
+    "FAError", "library_path", "load_library", "fa_fwd", "fa_bwd", "fa_bwd_deterministic", "fwd", "bwd",
     "bwd_workspace_size", "check_status", "attention", "FlashAttention", "version",
     "FA_BF16", "FA_FP32", "profile_enable", "profile_read",
 ]
@@ -70,6 +70,8 @@ def load_library():
         lib.fa_fwd.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_deterministic.argtypes = lib.fa_bwd.argtypes
+        lib.fa_bwd_deterministic.restype = i
         lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_get_last_error.argtypes = []
@@ -103,7 +105,7 @@ def version() -> int:
     return load_library().fa_version()
 
 
-PROFILE_KINDS = ("fwd", "bwd_preprocess", "bwd_main", "dq_convert")
+PROFILE_KINDS = ("fwd", "bwd_preprocess", "bwd_main", "dq_convert", "dq_pass")
 
 
 def profile_enable(on: bool = True):
@@ -113,8 +115,8 @@ def profile_enable(on: bool = True):
 
 def profile_read():
     """{kind: (total_ms, launches)} for the kernels timed since the last read."""
-    ms = (ctypes.c_double * 4)()
-    n = (ctypes.c_int * 4)()
+    ms = (ctypes.c_double * len(PROFILE_KINDS))()
+    n = (ctypes.c_int * len(PROFILE_KINDS))()
     _check(load_library().fa_profile_read(ms, n))
     return {k: (ms[i], n[i]) for i, k in enumerate(PROFILE_KINDS)}
 
@@ -161,6 +163,13 @@ def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, ws, ws_bytes, B, H, S, d, causal, sc
                                  int(causal), float(scale), dtype, stream)
 
 
+def fa_bwd_deterministic(q, k, v, o, dO, lse, dq, dk, dv, ws, ws_bytes, B, H, S, d, causal, scale, dtype,
+                         stream) -> int:
+    """Raw C-ABI call of the deterministic backward on device pointers; returns the status."""
+    return load_library().fa_bwd_deterministic(q, k, v, o, dO, lse, dq, dk, dv, ws, ws_bytes, B, H, S, d,
+                                               int(causal), float(scale), dtype, stream)
+
+
 def bwd_workspace_size(B: int, H: int, S: int, d: int, dtype) -> int:
     code = dtype if isinstance(dtype, int) else (FA_BF16 if dtype == torch.bfloat16 else FA_FP32)
     return int(load_library().fa_bwd_workspace_size(B, H, S, d, code))
@@ -186,9 +195,11 @@ def fwd(q, k, v, causal: bool = False, scale=None, out=None, lse=None, stream=No
 
 
 def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, stream=None,
-        out=None):
+        out=None, deterministic: bool = False):
     """Backward pass; returns (dq, dk, dv).  ``workspace`` (uint8, >= the size
-    reported by bwd_workspace_size) is allocated here when not given."""
+    reported by bwd_workspace_size) is allocated here when not given.
+    ``deterministic`` selects fa_bwd_deterministic: dQ from its own
+    query-tile-outer pass, bitwise reproducible."""
     _check_qkv(q, k, v, o, do)
     B, H, S, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -201,9 +212,10 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
     else:
         dq, dk, dv = out
     with torch.cuda.device(q.device):
-        rc = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                    _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                    B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
+        entry = fa_bwd_deterministic if deterministic else fa_bwd
+        rc = entry(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                   _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                   B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
     _check(rc)
     return dq, dk, dv
 
@@ -287,19 +299,22 @@ class FlashAttention(torch.autograd.Function):
     """O = softmax(Q K^T * scale) V with the recompute backward."""
 
     @staticmethod
-    def forward(ctx, q, k, v, is_causal=False, scale=None):
+    def forward(ctx, q, k, v, is_causal=False, scale=None, deterministic=False):
         o, lse = fwd(q, k, v, is_causal, scale)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.is_causal = bool(is_causal)
         ctx.scale = scale
+        ctx.deterministic = bool(deterministic)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, ctx.is_causal, ctx.scale)
-        return dq, dk, dv, None, None
+        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, ctx.is_causal, ctx.scale,
+                         deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None
 
 
-def attention(q, k, v, causal: bool = False, scale=None):
-    return FlashAttention.apply(q, k, v, causal, scale)
+def attention(q, k, v, causal: bool = False, scale=None, deterministic: bool = False):
+    """Differentiable attention; ``deterministic`` makes the backward bitwise reproducible."""
+    return FlashAttention.apply(q, k, v, causal, scale, deterministic)

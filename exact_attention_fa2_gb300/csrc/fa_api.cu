@@ -90,7 +90,7 @@ int check_ptr(const void* p, const char* name) {
 }
 
 // ---- optional kernel timing (fa_profile_enable / fa_profile_read)
-enum { PROF_FWD = 0, PROF_PRE = 1, PROF_BWD = 2, PROF_CONV = 3, PROF_KINDS = 4 };
+enum { PROF_FWD = 0, PROF_PRE = 1, PROF_BWD = 2, PROF_CONV = 3, PROF_DQ = 4, PROF_KINDS = 5 };
 struct ProfRec { cudaEvent_t a, b; int kind; };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
@@ -267,10 +267,16 @@ size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype) {
     return align_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-           const float* lse, void* dq, void* dk, void* dv,
-           void* workspace, size_t workspace_bytes,
-           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// fa_bwd and fa_bwd_deterministic: the same checks, D preprocess and dK/dV
+// loop; dQ either by atomics into dQacc plus a convert, or by its own
+// query-tile-outer pass.
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+               int B, int H, int S, int d, int causal, float scale, int dtype, void* stream, bool det) {
     g_err[0] = 0;
     int rc = check_sizes(B, H, S, d, scale, dtype);
     if (rc == 1) return FA_OK;
@@ -279,26 +285,55 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
         (rc = check_ptr(o, "o")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(lse, "lse")) ||
         (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
         return rc;
-    const size_t need = fa_bwd_workspace_size(B, H, S, d, dtype);
+    const size_t rows = (size_t)B * H * S;
+    const size_t need = det ? rows * sizeof(float) : fa_bwd_workspace_size(B, H, S, d, dtype);
     if (!workspace || workspace_bytes < need)
         return fail(FA_ERR_WORKSPACE, "workspace %p of %zu bytes, need %zu", workspace, workspace_bytes, need);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
-    const size_t rows = (size_t)B * H * S;
     float* Dvec = static_cast<float*>(workspace);
-    float* dQacc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * sizeof(float), 256));
+    float* dQacc = det ? nullptr
+                       : reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * sizeof(float), 256));
     fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, Dvec, dQacc, B, H, S, d, causal ? 1 : 0, scale,
                   dtype, static_cast<cudaStream_t>(stream), nullptr};
     if ((rc = status_ptr(&a.status))) return rc;
     cudaError_t e = timed(PROF_PRE, a.stream, [&] { return fa::launch_bwd_preprocess(a); });
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
     e = timed(PROF_BWD, a.stream, [&] {
-        return dtype == FA_BF16 ? fa::launch_bwd_tc(a) : fa::launch_bwd_simt(a);
+        if (dtype != FA_BF16) return fa::launch_bwd_simt(a);
+        return det ? fa::launch_bwd_tc_dkdv(a) : fa::launch_bwd_tc(a);
     });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    e = timed(PROF_CONV, a.stream, [&] { return fa::launch_dq_convert(a); });
-    if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
+    if (det) {
+        e = timed(PROF_DQ, a.stream, [&] {
+            return dtype == FA_BF16 ? fa::launch_bwd_dq_tc(a) : fa::launch_bwd_dq_simt(a);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "dq pass launch");
+    } else {
+        e = timed(PROF_CONV, a.stream, [&] { return fa::launch_dq_convert(a); });
+        if (e != cudaSuccess) return cuda_fail(e, "dq convert launch");
+    }
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+           const float* lse, void* dq, void* dk, void* dv,
+           void* workspace, size_t workspace_bytes,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, S, d, causal, scale,
+                      dtype, stream, false);
+}
+
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes,
+                         int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, S, d, causal, scale,
+                      dtype, stream, true);
 }
 
 size_t fa_fwd_bwd_host_buffer_size(int B, int H, int S, int d, int dtype) {

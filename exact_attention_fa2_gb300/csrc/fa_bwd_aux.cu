@@ -3,7 +3,8 @@
 // preprocess: D_i = rowsum(O * dO)_i in fp32 ("Stanford CS336 Assignment 2
 //   (Systems)" handout, section 4, "backward pass with recomputation": D is
 //   precomputed in global memory; Algorithm 2 step 2), and zeroing of the fp32
-//   dQ accumulator that the key-tile-outer kernel adds into.
+//   dQ accumulator that the key-tile-outer kernel adds into (skipped when
+//   there is none: the deterministic backward sums dQ in its own pass).
 // dq_convert: dq = dQacc * scale rounded to the storage dtype (Eq. 18's 1/sqrt(d)
 //   is applied here once instead of on every partial product).
 //
@@ -61,9 +62,12 @@ bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, float* 
 #pragma unroll
                     for (int i = 0; i < VN; ++i) part[u] = fmaf(a[i], b[i], part[u]);
                 }
-                // This row of the dQ accumulator starts at zero.
+                // This row of the dQ accumulator starts at zero (no accumulator
+                // in the deterministic backward).
+                if (z != nullptr) {
 #pragma unroll
-                for (int k = c; k < Z4; k += RG::G) z[row * Z4 + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = c; k < Z4; k += RG::G) z[row * Z4 + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
 #pragma unroll

@@ -140,48 +140,10 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
-// B operand of the products whose N dimension is the head dim: a [rows][d]
-// tile (TMA layout, 128 rows) read MN-major, k-step of 16 rows `ks`.
-// `b_lo` is the low descriptor word of the tile (LBO = the 64-column chunk
-// stride); the A operand is either Tensor Memory (`a_tm`) or shared memory
-// (`a_desc`).
-template <int D, bool A_TMEM>
-__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint64_t a_desc, uint32_t b_lo, int ks,
-                                           uint32_t a_mn, uint32_t acc) {
-    using C = Chunks<D>;
-    if constexpr (C::SINGLE_N) {
-        const uint64_t bdesc = desc_make(b_lo + ks * 128, desc_hi(1024, SW_128B));
-        if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, D, 0, 1), acc);
-        else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, D, a_mn, 1), acc);
-    } else {
-#pragma unroll
-        for (int c = 0; c < C::NCH; ++c) {
-            const uint32_t off = (C::tile_off(c, 128) + ks * 16 * C::row_bytes(c)) >> 4;
-            const uint64_t bdesc = desc_make(b_lo + off, desc_hi(8 * C::row_bytes(c), C::swz(c)));
-            if constexpr (A_TMEM) mma_ts(d_tmem + c * 64, a_tm, bdesc, idesc_bf16(128, C::width(c), 0, 1), acc);
-            else mma_ss(d_tmem + c * 64, a_desc, bdesc, idesc_bf16(128, C::width(c), a_mn, 1), acc);
-        }
-    }
-}
-
-// C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim
-// contiguous); a_lo / b_lo are the tiles' low descriptor words (LBO 16).
-template <int D>
-__device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
-    using C = Chunks<D>;
-    int step = 0;
-#pragma unroll
-    for (int c = 0; c < C::NCH; ++c) {
-#pragma unroll
-        for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
-            const uint32_t off = (C::tile_off(c, 128) + s * 32) >> 4;
-            const uint32_t hi = desc_hi(8 * C::row_bytes(c), C::swz(c));
-            mma_ss(d_tmem, desc_make(a_lo + off, hi), desc_make(b_lo + off, hi), idesc, step > 0 ? 1u : 0u);
-        }
-    }
-}
-
-template <int D>
+// WITH_DQ = false: dK and dV only (the deterministic backward computes dQ in
+// a separate query-tile-outer pass); the dQ warps then stay idle and the
+// buffers the dQ read-out would release are released by the MMA issuer.
+template <int D, bool WITH_DQ>
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
     using C = Chunks<D>;
     using QC = DqChunks<D>;
@@ -375,6 +337,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                                              (it > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
+                    if constexpr (!WITH_DQ) mma_commit(ds_free(it & 1));   // dK has read dS^T
+                }
+                if constexpr (!WITH_DQ) {
+                    __syncwarp();
+                    continue;
                 }
                 if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
                 tc_fence_after();
@@ -396,7 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);         // S^T = K Q^T
-            if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+            if (WITH_DQ && it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) {
                 mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
@@ -415,12 +382,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
                     mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                 }
+                if constexpr (WITH_DQ) {
 #pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks) {                                      // dQ_i = dS K
-                    const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
+                        const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
+                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(dq_full);
+                } else {
+                    mma_commit(q_empty(s));             // Q_i, dO_i (and L, D) are no longer read
                 }
-                mma_commit(dq_full);
             }
             __syncwarp();
         }
@@ -534,7 +505,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         }
-    } else {
+    } else if constexpr (WITH_DQ) {
         // ------------------------------------------------------------ dQ_i read-out and reduce-add
         const int wq = warp & 3;
         const int qr = wq * 32 + lane;                 // query row inside the tile
@@ -604,7 +575,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool WITH_DQ>
 cudaError_t bwd_tc_launch(const BwdArgs& a) {
     using C = Chunks<D>;
     using G = BwdCfg<D>;
@@ -619,7 +590,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
         if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess)
             return e;
     }
-    {
+    if (WITH_DQ) {
         using QC = DqChunks<D>;
         cudaError_t e;
         if (QC::N32 > 0 && (e = make_tmap_f32_3d(&p.tdq[0], a.dQacc, D, a.S, BH, 32, 128)) != cudaSuccess) return e;
@@ -638,24 +609,29 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     p.c = c < 1e-30f ? 1e-30f : c;
     p.scale = a.scale;
     p.neg_a = a.scale < 0.f ? 1u : 0u;
-    auto kern = bwd_tc_kernel<D>;
+    auto kern = bwd_tc_kernel<D, WITH_DQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_kv * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }
 
-}  // namespace
-
-cudaError_t launch_bwd_tc(const BwdArgs& a) {
+template <bool WITH_DQ>
+cudaError_t bwd_tc_dispatch(const BwdArgs& a) {
     switch (a.d) {
-        case 16: return bwd_tc_launch<16>(a);
-        case 32: return bwd_tc_launch<32>(a);
-        case 64: return bwd_tc_launch<64>(a);
-        case 80: return bwd_tc_launch<80>(a);
-        case 96: return bwd_tc_launch<96>(a);
-        case 128: return bwd_tc_launch<128>(a);
+        case 16: return bwd_tc_launch<16, WITH_DQ>(a);
+        case 32: return bwd_tc_launch<32, WITH_DQ>(a);
+        case 64: return bwd_tc_launch<64, WITH_DQ>(a);
+        case 80: return bwd_tc_launch<80, WITH_DQ>(a);
+        case 96: return bwd_tc_launch<96, WITH_DQ>(a);
+        case 128: return bwd_tc_launch<128, WITH_DQ>(a);
         default: return cudaErrorInvalidValue;
     }
 }
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs& a) { return bwd_tc_dispatch<true>(a); }
+
+cudaError_t launch_bwd_tc_dkdv(const BwdArgs& a) { return bwd_tc_dispatch<false>(a); }
 
 }  // namespace fa

@@ -35,7 +35,7 @@ struct BwdArgs {
     void* dk;
     void* dv;
     float* Dvec;            // [B*H*S] fp32, inside the workspace
-    float* dQacc;           // [B*H*S*d] fp32, inside the workspace
+    float* dQacc;           // [B*H*S*d] fp32, inside the workspace (null: deterministic backward)
     int B, H, S, d;
     int causal;
     float scale;
@@ -97,5 +97,11 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs& a);
 cudaError_t launch_bwd_tc(const BwdArgs& a);
+
+// Deterministic backward: dK/dV without dQ, then a query-tile-outer dQ pass
+// that writes dq directly (no dQacc, no atomics).
+cudaError_t launch_bwd_tc_dkdv(const BwdArgs& a);
+cudaError_t launch_bwd_dq_tc(const BwdArgs& a);
+cudaError_t launch_bwd_dq_simt(const BwdArgs& a);
 
 }  // namespace fa

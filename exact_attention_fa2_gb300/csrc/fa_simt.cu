@@ -14,7 +14,8 @@
 // Backward (same handout, Eq. 13-19 and Algorithm 2, key-tile-outer part):
 // one CTA per (64-key tile, batch*head) accumulates dK and dV in registers
 // over all query tiles at or below the diagonal; dQ contributions of every
-// key tile are added with fp32 atomics into the dQ accumulator.
+// key tile are added with fp32 atomics into the dQ accumulator, or, for the
+// deterministic backward, summed by a separate query-tile-outer pass.
 
 #include "fa_common.cuh"
 #include "fa_launch.h"
@@ -303,7 +304,9 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
                 }
         }
 
-        // dQ_i += dS K (Eq. 18, scale applied when dQacc is converted).
+        // dQ_i += dS K (Eq. 18, scale applied when dQacc is converted); the
+        // deterministic backward (no dQacc) sums dQ in its own pass instead.
+        if (dQacc == nullptr) continue;
         float dq[4][NC];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -345,6 +348,113 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     }
 }
 
+// Deterministic dQ pass (Algorithm 2's separate query-tile-outer loop): one
+// CTA per (64-row query tile, batch*head) recomputes S, P, dP and dS for every
+// key tile at or below the diagonal and sums dQ = dS K in registers in key
+// order, so every dQ element has one fixed summation order and no atomics.
+template <typename T, int D>
+__global__ void __launch_bounds__(NT)
+bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const T* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ Dvec,
+                   T* __restrict__ dq, int S, int causal, float scale, float scale_log2) {
+    extern __shared__ float smem[];
+    constexpr int LD = D + 1;
+    constexpr int NC = D / 16;
+    float* Ks = smem;
+    float* Vs = Ks + 64 * LD;
+    float* Qs = Vs + 64 * LD;
+    float* dOs = Qs + 64 * LD;
+    float* dSs = dOs + 64 * LD;          // [query][key]
+    float* L2s = dSs + 64 * LDP;
+    float* Ds = L2s + 64;
+
+    const int tid = threadIdx.x;
+    const int ty = tid / 16, tx = tid % 16;
+    const int n_q = (S + BQ - 1) / BQ;
+    const int qt = causal ? n_q - 1 - (int)blockIdx.x : (int)blockIdx.x;   // longest rows first
+    const int q0 = qt * BQ;
+    const size_t bh = blockIdx.y;
+    const size_t base = bh * S * D;
+
+    load_tile<T, D>(Qs, LD, q + base, q0, S);
+    load_tile<T, D>(dOs, LD, dO + base, q0, S);
+    if (tid < 64) {
+        const int row = q0 + tid;
+        L2s[tid] = row < S ? lse[bh * S + row] * FA_LOG2E : INFINITY;
+        Ds[tid] = row < S ? Dvec[bh * S + row] : 0.f;
+    }
+    float acc[4][NC];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
+
+    const int n_k = causal ? qt + 1 : (S + BK - 1) / BK;
+    for (int kt = 0; kt < n_k; ++kt) {
+        const int k0 = kt * BK;
+        __syncthreads();
+        load_tile<T, D>(Ks, LD, k + base, k0, S);
+        load_tile<T, D>(Vs, LD, v + base, k0, S);
+        __syncthreads();
+        // S, dP (Eq. 13, 16): rows queries ty*4+r, columns keys tx+16c.
+        float s[4][4], dp[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) { s[r][c] = 0.f; dp[r][c] = 0.f; }
+#pragma unroll 4
+        for (int kk = 0; kk < D; ++kk) {
+            float qa[4], da[4], kb[4], vb[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) { qa[r] = Qs[(ty * 4 + r) * LD + kk]; da[r] = dOs[(ty * 4 + r) * LD + kk]; }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) { kb[c] = Ks[(tx + 16 * c) * LD + kk]; vb[c] = Vs[(tx + 16 * c) * LD + kk]; }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    s[r][c] = fmaf(qa[r], kb[c], s[r][c]);
+                    dp[r][c] = fmaf(da[r], vb[c], dp[r][c]);
+                }
+        }
+        // P, dS (Eq. 14, 17).
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int lr = ty * 4 + r;
+            const int row = q0 + lr;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col = k0 + tx + 16 * c;
+                const bool keep = col < S && row < S && (!causal || col <= row);
+                const float pr = keep ? exp2f(fmaf(s[r][c], scale_log2, -L2s[lr])) : 0.f;
+                dSs[lr * LDP + tx + 16 * c] = round_to<T>(pr * (dp[r][c] - Ds[lr]));
+            }
+        }
+        __syncthreads();
+        // dQ_i += dS K_j (Eq. 18): rows queries ty*4+r, columns d tx+16c.
+#pragma unroll 4
+        for (int kk = 0; kk < BK; ++kk) {
+            float sa[4], kb[NC];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sa[r] = dSs[(ty * 4 + r) * LDP + kk];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) kb[c] = Ks[kk * LD + tx + 16 * c];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < NC; ++c) acc[r][c] = fmaf(sa[r], kb[c], acc[r][c]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int row = q0 + ty * 4 + r;
+        if (row < S) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) dq[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(acc[r][c] * scale);
+        }
+    }
+}
+
 template <typename T, int D>
 cudaError_t fwd_simt_launch(const FwdArgs& a, int kb, int ke, T* o) {
     constexpr size_t smem = fwd_smem_bytes<D>();
@@ -369,6 +479,31 @@ cudaError_t bwd_simt_launch(const BwdArgs& a) {
                                        a.lse, a.Dvec, a.dQacc, (T*)a.dk, (T*)a.dv, a.S, a.causal,
                                        a.scale, a.scale * FA_LOG2E);
     return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t bwd_dq_simt_launch(const BwdArgs& a) {
+    constexpr size_t smem = sizeof(float) * (size_t)(64 * (D + 1) * 4 + 64 * LDP + 2 * 64);
+    auto kern = bwd_dq_simt_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.S + BQ - 1) / BQ, a.B * a.H);
+    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.dO, a.lse,
+                                       a.Dvec, (T*)a.dq, a.S, a.causal, a.scale, a.scale * FA_LOG2E);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t bwd_dq_simt_dispatch(const BwdArgs& a) {
+    switch (a.d) {
+        case 16: return bwd_dq_simt_launch<T, 16>(a);
+        case 32: return bwd_dq_simt_launch<T, 32>(a);
+        case 64: return bwd_dq_simt_launch<T, 64>(a);
+        case 80: return bwd_dq_simt_launch<T, 80>(a);
+        case 96: return bwd_dq_simt_launch<T, 96>(a);
+        case 128: return bwd_dq_simt_launch<T, 128>(a);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <typename T>
@@ -412,6 +547,10 @@ cudaError_t launch_fwd_simt_partial(const FwdArgs& a, int key_begin, int key_end
 
 cudaError_t launch_bwd_simt(const BwdArgs& a) {
     return a.dtype == DT_FP32 ? bwd_simt_dispatch<float>(a) : bwd_simt_dispatch<__nv_bfloat16>(a);
+}
+
+cudaError_t launch_bwd_dq_simt(const BwdArgs& a) {
+    return a.dtype == DT_FP32 ? bwd_dq_simt_dispatch<float>(a) : bwd_dq_simt_dispatch<__nv_bfloat16>(a);
 }
 
 }  // namespace fa

@@ -1,6 +1,7 @@
 // fa_tc_common.cuh - pieces shared by the tensor-core forward and backward
 // kernels: head-dimension chunking for TMA boxes and MMA descriptors, warp
-// waits and register fences for Tensor Memory loads.
+// waits, register fences for Tensor Memory loads, and the two product shapes
+// (N = head dim, K = head dim) issued on 128-row tiles.
 #pragma once
 
 #include "sm103_ptx.cuh"
@@ -51,6 +52,47 @@ template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t* r) {
 #pragma unroll
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// B operand of the products whose N dimension is the head dim: a [rows][d]
+// tile (TMA layout, 128 rows) read MN-major, k-step of 16 rows `ks`.
+// `b_lo` is the low descriptor word of the tile (LBO = the 64-column chunk
+// stride); the A operand is either Tensor Memory (`a_tm`) or shared memory
+// (`a_desc`).
+template <int D, bool A_TMEM>
+__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint64_t a_desc, uint32_t b_lo, int ks,
+                                           uint32_t a_mn, uint32_t acc) {
+    using C = Chunks<D>;
+    if constexpr (C::SINGLE_N) {
+        const uint64_t bdesc = desc_make(b_lo + ks * 128, desc_hi(1024, SW_128B));
+        if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, D, 0, 1), acc);
+        else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, D, a_mn, 1), acc);
+    } else {
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+            const uint32_t off = (C::tile_off(c, 128) + ks * 16 * C::row_bytes(c)) >> 4;
+            const uint64_t bdesc = desc_make(b_lo + off, desc_hi(8 * C::row_bytes(c), C::swz(c)));
+            if constexpr (A_TMEM) mma_ts(d_tmem + c * 64, a_tm, bdesc, idesc_bf16(128, C::width(c), 0, 1), acc);
+            else mma_ss(d_tmem + c * 64, a_desc, bdesc, idesc_bf16(128, C::width(c), a_mn, 1), acc);
+        }
+    }
+}
+
+// C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim
+// contiguous); a_lo / b_lo are the tiles' low descriptor words (LBO 16).
+template <int D>
+__device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
+    using C = Chunks<D>;
+    int step = 0;
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c) {
+#pragma unroll
+        for (int s = 0; s < C::width(c) / 16; ++s, ++step) {
+            const uint32_t off = (C::tile_off(c, 128) + s * 32) >> 4;
+            const uint32_t hi = desc_hi(8 * C::row_bytes(c), C::swz(c));
+            mma_ss(d_tmem, desc_make(a_lo + off, hi), desc_make(b_lo + off, hi), idesc, step > 0 ? 1u : 0u);
+        }
+    }
 }
 
 }  // namespace tc

@@ -137,6 +137,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * Deterministic backward: the same results as fa_bwd up to rounding, and
+ * bitwise identical from run to run.  Algorithm 2 of the handout as it is
+ * written: the key-tile-outer loop computes dK and dV only, and a separate
+ * query-tile-outer loop recomputes P, dP and dS to sum each dQ row in one
+ * fixed order (Eq. 18), with no atomics and no dQ accumulator.  It does more
+ * arithmetic than fa_bwd (S and dP are formed twice per tile pair).
+ *   Arguments as fa_bwd; dk and dv are bitwise equal to fa_bwd's.
+ *   workspace  device buffer of >= B*H*S*4 bytes (fa_bwd_workspace_size() is
+ *              always enough), 256-byte aligned; D is left at its start.
+ */
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes,
+                         int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/*
  * Backward pass for callers that cannot allocate device memory.
  * The pages describe no counterpart of this entry point; it exists for users
  * of this library that cannot call cudaMalloc (or any allocating routine,
@@ -213,12 +229,12 @@ int fa_version(void);
 
 /*
  * Kernel timing for benchmarks (not needed to compute attention).  While
- * enabled, every fa_fwd / fa_bwd call records a pair of CUDA events on its
+ * enabled, every fa_fwd / fa_bwd / fa_bwd_deterministic call records a pair of CUDA events on its
  * stream directly around each of its kernels.  fa_profile_read waits for the
  * recorded events, adds their elapsed times since the previous read into
- * ms[4] and the number of timed launches into launches[4], indexed by
+ * ms[5] and the number of timed launches into launches[5], indexed by
  *   0 = forward kernel, 1 = backward preprocess (D, dQacc zeroing),
- *   2 = backward main kernel, 3 = dQ conversion,
+ *   2 = backward main kernel, 3 = dQ conversion, 4 = deterministic dQ pass,
  * and forgets them.  Both return FA_OK or FA_ERR_CUDA / FA_ERR_INVALID_ARG.
  * Events come from a host-side pool; no device memory is allocated.
  */

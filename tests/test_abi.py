@@ -109,3 +109,18 @@ def test_partial_and_merge_argument_errors_need_no_gpu(lib):
     mrg = lambda **kw: lib.fa_merge(P, P, kw.get("o_b", P), P, P, P, 1, 2, 512, kw.get("d", 64), fa.FA_BF16, None)
     assert mrg(o_b=ctypes.c_void_p(0)) == -1
     assert mrg(d=48) == -2
+
+
+def test_deterministic_bwd_workspace_rules_need_no_gpu(lib):
+    """The deterministic backward needs only D (B*H*S fp32) as workspace and
+    checks it, and the pointers, before launching anything."""
+    P = ctypes.c_void_p(A)
+    B, H, S, d = 1, 2, 128, 64
+    det = lambda ws, nbytes, **kw: fa.fa_bwd_deterministic(P, P, P, P, P, P, kw.get("dq", P), P, P, ws, nbytes,
+                                                          B, H, S, kw.get("d", d), 1, 0.125, 0, None)
+    assert det(P, B * H * S * 4 - 1) == -4 and b"need 1024" in lib.fa_get_last_error()
+    assert det(ctypes.c_void_p(A + 16), B * H * S * 4) == -3
+    assert det(P, B * H * S * 4, dq=ctypes.c_void_p(0)) == -1
+    assert det(P, B * H * S * 4, d=48) == -2
+    assert fa.fa_bwd_deterministic(None, None, None, None, None, None, None, None, None, None, 0,
+                                   0, 2, 128, 64, 1, 0.125, 0, None) == 0

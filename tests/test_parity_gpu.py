@@ -382,3 +382,71 @@ def test_split_kv_merge_equals_full_attention(dtype, d):
         ref_o, _, _, ref_L = oracle.merge_two_halves(oa, ma, Ba, ob, mb, Bb)
         assert_close("O merged vs oracle", o[b, h].cpu(), ref_o, *tol["o"])
         assert_close("L merged vs oracle", lse[b, h].cpu(), ref_L, *tol["lse"])
+
+
+def _bwd_both(q, k, v, do, causal, scale):
+    """Forward once, then the atomic backward once and the deterministic
+    backward twice (the second on a fresh, garbage-filled workspace)."""
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal, scale)
+    atomic = fa.bwd(qd, kd, vd, o, dod, lse, causal, scale)
+    dets = []
+    for fill in (0, 0x7F):
+        B, H, S, d = q.shape
+        ws = torch.full((B * H * S * 4,), fill, device=DEV, dtype=torch.uint8)
+        dets.append(fa.bwd(qd, kd, vd, o, dod, lse, causal, scale, workspace=ws, deterministic=True))
+    fa.check_status()
+    cpu = lambda ts: [t.cpu() for t in ts]
+    return cpu(atomic), cpu(dets[0]), cpu(dets[1])
+
+
+@pytest.mark.parametrize("dtype,d,S,causal,scale", [
+    ("bf16", 64, 333, True, None), ("bf16", 128, 640, False, None), ("bf16", 80, 300, True, None),
+    ("bf16", 96, 257, False, None), ("bf16", 16, 200, True, None), ("bf16", 32, 129, False, -0.3),
+    ("bf16", 128, 1, True, None), ("fp32", 32, 200, True, None), ("fp32", 64, 129, False, 0.05),
+])
+def test_deterministic_backward_matches_oracle_and_repeats_bitwise(dtype, d, S, causal, scale):
+    """Algorithm 2's separate dQ loop: every gradient within the tolerance of
+    the oracle, dK and dV bitwise equal to the atomic backward's (the same
+    key-tile-outer arithmetic), and all three bitwise equal across runs."""
+    q, k, v, do = make_inputs(2, 2, S, d, dtype, seed=8100 + d + S)
+    scale = 1 / math.sqrt(d) if scale is None else scale
+    atomic, det1, det2 = _bwd_both(q, k, v, do, causal, scale)
+    for name, a, b in zip(("dq", "dk", "dv"), det1, det2):
+        assert torch.equal(a, b), f"{name} differs between deterministic runs"
+    assert torch.equal(det1[1], atomic[1]), "dk differs from the atomic backward"
+    assert torch.equal(det1[2], atomic[2]), "dv differs from the atomic backward"
+    tol = TOL[dtype]
+    assert_close("dq vs atomic backward", det1[0], f64(atomic[0]), *tol["grad"])
+    for (b, h) in all_heads(2, 2):
+        r = oracle_head(q, k, v, do, b, h, causal, scale, dtype)
+        for name, g in zip(("dq", "dk", "dv"), det1):
+            assert_close(f"{name} deterministic [b={b},h={h}]", g[b, h], r[name], *tol["grad"])
+
+
+def test_deterministic_backward_c2_sampled_heads():
+    """The deterministic backward at the full c2 workload size (4x12x1024,
+    d=64, causal), sampled heads against the oracle, and repeat-exact."""
+    w = WORKLOADS["c2"]
+    q, k, v, do = make_workload_inputs(w)
+    scale = 1 / math.sqrt(w.d)
+    atomic, det1, det2 = _bwd_both(q, k, v, do, True, scale)
+    for a, b in zip(det1, det2):
+        assert torch.equal(a, b)
+    assert torch.equal(det1[1], atomic[1]) and torch.equal(det1[2], atomic[2])
+    for (b, h) in [(0, 0), (1, 5), (3, 11)]:
+        r = oracle_head(q, k, v, do, b, h, True, scale, "bf16")
+        for name, g in zip(("dq", "dk", "dv"), det1):
+            assert_close(f"{name} deterministic [b={b},h={h}]", g[b, h], r[name], *TOL["bf16"]["grad"])
+
+
+def test_deterministic_autograd_matches_atomic():
+    q, k, v, do = make_inputs(1, 2, 384, 64, "bf16", seed=8200)
+    grads = []
+    for det in (False, True):
+        qd, kd, vd = (t.to(DEV).requires_grad_(True) for t in (q, k, v))
+        out = fa.attention(qd, kd, vd, True, None, deterministic=det)
+        out.backward(do.to(DEV))
+        grads.append([t.grad.cpu() for t in (qd, kd, vd)])
+    assert torch.equal(grads[0][1], grads[1][1]) and torch.equal(grads[0][2], grads[1][2])
+    assert_close("dq", grads[1][0], f64(grads[0][0]), *TOL["bf16"]["grad"])
