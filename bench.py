@@ -307,6 +307,37 @@ def run_ours(args, world, rank, local):
     fa.check_status()
     launches_per_step = sum(v[1] for v in prof.values()) / prof_steps
 
+    # The same step with the deterministic backward (fa_bwd_deterministic:
+    # dK/dV-only kernel plus the query-tile-outer dQ pass), timed the same way
+    # after the main measurement, and its kernels from the library's events.
+    def step_det():
+        fa.fwd(qd, kd, vd, causal, scale, out=od, lse=lsed)
+        fa.bwd(qd, kd, vd, od, dod, lsed, causal, scale, workspace=ws, out=(dqd, dkd, dvd), deterministic=True)
+
+    for _ in range(3):
+        step_det()
+    det_steps = max(5, min(args.steps, 50))
+    ev_det = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(det_steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(det_steps):
+        flush.zero_()
+        ev_det[i][0].record(stream)
+        step_det()
+        ev_det[i][1].record(stream)
+    torch.cuda.synchronize()
+    fa.check_status()
+    det_ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_det) / det_steps, world)
+    fa.profile_read()
+    fa.profile_enable(True)
+    for i in range(5):
+        flush.zero_()
+        step_det()
+    torch.cuda.synchronize()
+    fa.profile_enable(False)
+    prof_det = fa.profile_read()
+    fa.check_status()
+
     # End to end through the C ABI with host buffers (fa_fwd_bwd_host): every
     # step copies q, k, v, dO from pinned host memory, runs forward and
     # backward, and copies o, lse, dq, dk, dv back.  Steps rotate over three
@@ -398,6 +429,13 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": kernel_names[dom], "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst"},
+        "deterministic_bwd": {
+            "api": "fa_bwd_deterministic (Algorithm 2's separate dQ loop, no atomics)",
+            "ms_per_step": det_ms_per_step,
+            "value": world * step_flops / (det_ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "dkdv_ms": (prof_det["bwd_main"][0] / prof_det["bwd_main"][1]) if prof_det["bwd_main"][1] else None,
+            "dq_pass_ms": (prof_det["dq_pass"][0] / prof_det["dq_pass"][1]) if prof_det["dq_pass"][1] else None,
+            "steps": det_steps},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "fa_fwd_bwd_host (host buffers)", "pipelining": f"steps rotate over {NR} streams"},
