@@ -3,9 +3,12 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring): the CUDA library never
 imports this module, and this module imports nothing from the library.
 
-Layout: every 4-D array is [B, H, S, d] (float64), L and D are [B, H, S].
-Self-attention only: N_q = N_k = S.  Inputs are widened exactly to float64 by
-the caller from the values the GPU sees (bf16- or fp32-rounded).
+Layout: every 4-D array is [B, H, N, d] (float64) with N = N_q for Q, O, dO
+and N = N_k for K, V (Algorithms 1 and 2 of the handout take Q in R^{N_q x d}
+and K, V in R^{N_k x d}); L and D are [B, H, N_q].  Under the causal mask key j
+is kept for query i when j <= i, whatever N_q and N_k are.  Inputs are widened
+exactly to float64 by the caller from the values the GPU sees (bf16- or
+fp32-rounded).
 """
 from __future__ import annotations
 
@@ -60,14 +63,14 @@ def _softmax_and_lse(S: np.ndarray, keep):
 def attention_fwd(q, k, v, causal: bool, scale: float):
     """O = softmax(Q K^T * scale) V and L = logsumexp of the scaled scores.
 
-    Handout Eq. 4-6 and Eq. 12, one (b, h) slice at a time, full S x S matrix.
-    Returns (O [B,H,S,d], L [B,H,S]).
+    Handout Eq. 4-6 and Eq. 12, one (b, h) slice at a time, full N_q x N_k
+    matrix.  Returns (O [B,H,N_q,d], L [B,H,N_q]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    B, H, S, d = q.shape
-    keep = causal_keep(S, S) if causal else None
+    B, H, Nq, d = q.shape
+    keep = causal_keep(Nq, k.shape[2]) if causal else None
     O = np.empty_like(q)
-    L = np.empty((B, H, S))
+    L = np.empty((B, H, Nq))
     for b in range(B):
         for h in range(H):
             P, Lbh = _softmax_and_lse(scores(q[b, h], k[b, h], scale), keep)
@@ -104,8 +107,8 @@ def attention_bwd(q, k, v, do, causal: bool, scale: float):
     separately that P_i . dP_i equals D_i = rowsum(O * dO)_i.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
-    B, H, S, d = q.shape
-    keep = causal_keep(S, S) if causal else None
+    B, H, Nq, d = q.shape
+    keep = causal_keep(Nq, k.shape[2]) if causal else None
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
@@ -134,8 +137,8 @@ def attention_bwd_from_output(q, k, v, o, do, L, causal: bool, scale: float):
       dQ = dS K * scale (Eq. 18),  dK = dS^T Q * scale (Eq. 19).
     """
     q, k, v, o, do, L = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do), _f64(L)
-    B, H, S, d = q.shape
-    keep = causal_keep(S, S) if causal else None
+    B, H, Nq, d = q.shape
+    keep = causal_keep(Nq, k.shape[2]) if causal else None
     D = rowsum_o_do(o, do)
     dq = np.empty_like(q)
     dk = np.empty_like(k)

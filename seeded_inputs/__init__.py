@@ -22,7 +22,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "sweep_points", "seed_for"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_inputs_rect", "sweep_points", "seed_for"]
 
 
 @dataclass(frozen=True)
@@ -90,6 +90,17 @@ def make_inputs(B: int, H: int, S: int, d: int, dtype: str = "bf16", seed: int =
         x.mul_(qkv_scale if i < 3 else do_scale)
         out.append(x.to(tdt).contiguous())
     return tuple(out)
+
+
+def make_inputs_rect(B: int, H: int, Sq: int, Sk: int, d: int, dtype: str = "bf16", seed: int = 0):
+    """(Q, K, V, dO) for N_q = Sq queries and N_k = Sk keys: Q, dO of shape
+    [B, H, Sq, d] and K, V of shape [B, H, Sk, d], N(0,1) draws in the order
+    Q, K, V, dO from one seeded generator, rounded to ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    tdt = torch_dtype(dtype)
+    shapes = ((B, H, Sq, d), (B, H, Sk, d), (B, H, Sk, d), (B, H, Sq, d))
+    return tuple(torch.randn(sh, generator=g, dtype=torch.float32).to(tdt).contiguous() for sh in shapes)
 
 
 def make_workload_inputs(w: Workload):

@@ -303,3 +303,91 @@ def test_round_to_bf16_matches_torch():
     x = rnd(150, 100000) * np.exp(rnd(151, 100000) * 5)
     ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
     np.testing.assert_array_equal(oracle.round_to_storage(x, "bf16"), ref)
+
+
+# ---------------------------------------------------------------- N_q != N_k (Algorithms 1 and 2: Q has N_q rows, K, V have N_k)
+def _brute_fwd_rect(Q, K, V, causal, sc):
+    """Plain loops over N_q query rows and N_k keys; causal keeps key j <= i."""
+    O, L = [], []
+    for i in range(len(Q)):
+        js = [j for j in range(len(K)) if (j <= i or not causal)]
+        s = {j: sc * sum(a * b for a, b in zip(Q[i], K[j])) for j in js}
+        den = sum(math.exp(s[j]) for j in js)
+        O.append([sum(math.exp(s[j]) / den * V[j][t] for j in js) for t in range(len(V[0]))])
+        L.append(math.log(den))
+    return np.array(O), np.array(L)
+
+
+@pytest.mark.parametrize("nq,nk", [(3, 7), (7, 3), (5, 5)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_forward_matches_brute_force_loops(nq, nk, causal):
+    d, sc = 3, 0.65
+    q, k, v = rnd(300 + nq, 1, 1, nq, d), rnd(310 + nk, 1, 1, nk, d), rnd(320 + nk, 1, 1, nk, d)
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    assert O.shape == (1, 1, nq, d) and L.shape == (1, 1, nq)
+    Ob, Lb = _brute_fwd_rect(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), causal, sc)
+    np.testing.assert_allclose(O[0, 0], Ob, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(L[0, 0], Lb, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("nq,nk", [(3, 6), (6, 2)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_gradients_finite_differences(nq, nk, causal):
+    """Both backward forms against central differences of sum(W * O) for N_q != N_k."""
+    d, sc, hh = 3, 0.55, 1e-6
+    q, w = rnd(330, 1, 1, nq, d), rnd(331, 1, 1, nq, d)
+    k, v = rnd(332, 1, 1, nk, d), rnd(333, 1, 1, nk, d)
+    g_std = oracle.attention_bwd(q, k, v, w, causal, sc)
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    g_rec = oracle.attention_bwd_from_output(q, k, v, O, w, L, causal, sc)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(w * oracle.attention_fwd(q_, k_, v_, causal, sc)[0]))
+
+    for which, n in ((0, nq), (1, nk), (2, nk)):
+        num = np.zeros((n, d))
+        for i in range(n):
+            for t in range(d):
+                ap = [q.copy(), k.copy(), v.copy()]
+                am = [q.copy(), k.copy(), v.copy()]
+                ap[which][0, 0, i, t] += hh
+                am[which][0, 0, i, t] -= hh
+                num[i, t] = (loss(*ap) - loss(*am)) / (2 * hh)
+        np.testing.assert_allclose(g_std[which][0, 0], num, rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(g_rec[which][0, 0], num, rtol=1e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("nq,nk", [(9, 20), (20, 9)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rectangular_torch_sdpa_fp64_cross_check(nq, nk, causal):
+    """PyTorch's scaled_dot_product_attention aligns is_causal top-left
+    (keep j <= i) for N_q != N_k, the reading taken here."""
+    torch = pytest.importorskip("torch")
+    d, sc = 8, 0.3
+    q, do = rnd(340, 2, 2, nq, d), rnd(341, 2, 2, nq, d)
+    k, v = rnd(342, 2, 2, nk, d), rnd(343, 2, 2, nk, d)
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    dq, dk, dv = oracle.attention_bwd_from_output(q, k, v, O, do, L, causal, sc)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=sc)
+    to.backward(torch.tensor(do))
+    np.testing.assert_allclose(O, to.detach().numpy(), atol=1e-12)
+    for a, t in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-12)
+
+
+def test_rectangular_causal_keys_past_the_last_query_get_no_gradient():
+    """Top-left causal with N_k > N_q: keys j >= N_q are never attended, so
+    their dK and dV are exactly zero and removing them changes nothing."""
+    nq, nk, d, sc = 4, 9, 3, 0.5
+    q, do = rnd(350, 1, 1, nq, d), rnd(351, 1, 1, nq, d)
+    k, v = rnd(352, 1, 1, nk, d), rnd(353, 1, 1, nk, d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, True, sc)
+    assert np.all(dk[0, 0, nq:] == 0) and np.all(dv[0, 0, nq:] == 0)
+    O, L = oracle.attention_fwd(q, k, v, True, sc)
+    O2, L2 = oracle.attention_fwd(q, k[:, :, :nq], v[:, :, :nq], True, sc)
+    np.testing.assert_allclose(O, O2, atol=1e-15)
+    np.testing.assert_allclose(L, L2, atol=1e-15)
+    dq2, dk2, dv2 = oracle.attention_bwd(q, k[:, :, :nq], v[:, :, :nq], do, True, sc)
+    np.testing.assert_allclose(dq, dq2, atol=1e-15)
+    np.testing.assert_allclose(dk[:, :, :nq], dk2, atol=1e-15)
