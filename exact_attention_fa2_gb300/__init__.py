@@ -92,6 +92,10 @@ def load_library():
         lib.fa_fwd_bwd_host_buffer_size.restype = sz
         lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_bwd_host.restype = i
+        lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_strided.restype = i
+        lib.fa_bwd_strided.argtypes = ([vp] * 17 + [vp, sz] + [i, i, i, i, i, i, f, i, i, vp])
+        lib.fa_bwd_strided.restype = i
         _lib = lib
     return _lib
 
@@ -140,16 +144,31 @@ def _ptr(t):
 
 
 def _check_qkv(*ts):
+    """q, k, v (then o, dO): [B, H, N, d] CUDA tensors of one dtype and device
+    with a contiguous head dimension; q (o, dO) share N_q, k and v share N_k.
+    Other strides are passed to the library, which checks their alignment."""
     q = ts[0]
-    for t in ts:
-        if not t.is_cuda:
-            raise ValueError("tensors must be on a CUDA device (there is no CPU fallback)")
-        if not t.is_contiguous():
-            raise ValueError("tensors must be contiguous [B, H, S, d]")
-        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
-            raise ValueError("q, k, v (and o, dO) must share shape, dtype and device")
     if q.dim() != 4:
         raise ValueError("expected [B, H, S, d] tensors")
+    for i, t in enumerate(ts):
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device (there is no CPU fallback)")
+        if t.dtype != q.dtype or t.device != q.device or t.dim() != 4:
+            raise ValueError("q, k, v (and o, dO) must share dtype, device and rank 4")
+        if t.stride(-1) != 1:
+            raise ValueError("the head dimension (last) must be contiguous")
+        ref = q if i in (0, 3, 4) else ts[1]
+        if t.shape != ref.shape or t.shape[0] != q.shape[0] or t.shape[1] != q.shape[1] or t.shape[3] != q.shape[3]:
+            raise ValueError("q, o, dO must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
+
+
+def _plain(*ts):
+    """True when the plain (contiguous, N_q = N_k) entry points apply."""
+    return all(t.is_contiguous() for t in ts) and ts[0].shape == ts[1].shape
+
+
+def _strides(t):
+    return (ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2))
 
 
 def fa_fwd(q, k, v, o, lse, B, H, S, d, causal, scale, dtype, stream) -> int:
@@ -184,12 +203,22 @@ def fwd(q, k, v, causal: bool = False, scale=None, out=None, lse=None, stream=No
     """Forward pass; returns (o, lse)."""
     _check_qkv(q, k, v)
     B, H, S, d = q.shape
+    Sk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32) if lse is None else lse
+    _check_qkv(q, k, v, o)
+    if not lse.is_contiguous() or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S):
+        raise ValueError("lse must be a contiguous fp32 [B, H, N_q] tensor")
+    st = ctypes.c_void_p(_stream_handle(stream))
     with torch.cuda.device(q.device):
-        rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, d, causal, scale,
-                    _dtype_code(q), ctypes.c_void_p(_stream_handle(stream)))
+        if _plain(q, k, v, o):
+            rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, d, causal, scale,
+                        _dtype_code(q), st)
+        else:
+            rc = load_library().fa_fwd_strided(
+                _ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o), _strides(o), _ptr(lse),
+                B, H, S, Sk, d, int(causal), scale, _dtype_code(q), st)
     _check(rc)
     return o, lse
 
@@ -202,6 +231,7 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
     query-tile-outer pass, bitwise reproducible."""
     _check_qkv(q, k, v, o, do)
     B, H, S, d = q.shape
+    Sk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = _dtype_code(q)
     need = bwd_workspace_size(B, H, S, d, code)
@@ -211,11 +241,21 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
+    _check_qkv(q, k, v, o, do)
+    _check_qkv(dq, dk, dv, q, q)
+    st = ctypes.c_void_p(_stream_handle(stream))
+    nbytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
-        entry = fa_bwd_deterministic if deterministic else fa_bwd
-        rc = entry(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                   _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                   B, H, S, d, causal, scale, code, ctypes.c_void_p(_stream_handle(stream)))
+        if _plain(q, k, v, o, do, dq, dk, dv):
+            entry = fa_bwd_deterministic if deterministic else fa_bwd
+            rc = entry(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                       _ptr(dv), _ptr(workspace), nbytes, B, H, S, d, causal, scale, code, st)
+        else:
+            rc = load_library().fa_bwd_strided(
+                _ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o), _strides(o),
+                _ptr(do), _strides(do), _ptr(lse), _ptr(dq), _strides(dq), _ptr(dk), _strides(dk),
+                _ptr(dv), _strides(dv), _ptr(workspace), nbytes, B, H, S, Sk, d, int(causal), scale, code,
+                int(bool(deterministic)), st)
     _check(rc)
     return dq, dk, dv
 
@@ -225,6 +265,8 @@ def fwd_partial(q, k, v, key_begin: int, key_end: int, causal: bool = False, sca
     positions are whole-sequence positions); returns (o_part fp32, lse_part
     fp32), with o = 0 and lse = -inf where a query has no admissible key."""
     _check_qkv(q, k, v)
+    if not _plain(q, k, v):
+        raise ValueError("fwd_partial takes contiguous q, k, v of one length")
     B, H, S, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:

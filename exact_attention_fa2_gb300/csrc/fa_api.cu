@@ -89,6 +89,41 @@ int check_ptr(const void* p, const char* name) {
     return FA_OK;
 }
 
+// The view of a [B, H, rows, d] array from a host array of element strides
+// {batch, head, row} (NULL: contiguous).  A stride whose dimension has more
+// than one index must be positive and a multiple of 16 bytes.
+int get_view(const long long* st, int B, int H, int rows, int d, int dtype, const char* name, fa::View* out) {
+    if (!st) {
+        *out = fa::contiguous_view(H, rows, d);
+        return FA_OK;
+    }
+    const long long elt = dtype == FA_BF16 ? 2 : 4;
+    const int ext[3] = {B, H, rows};
+    static const char* dims[3] = {"batch", "head", "row"};
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] <= 1) continue;
+        if (st[i] <= 0)
+            return fail(FA_ERR_INVALID_ARG, "%s %s stride %lld is not positive", name, dims[i], st[i]);
+        if ((st[i] * elt) % 16 != 0 || st[i] * elt >= (1LL << 40))
+            return fail(FA_ERR_MISALIGNED, "%s %s stride %lld elements is not a multiple of 16 bytes (or too large)",
+                        name, dims[i], st[i]);
+    }
+    *out = fa::View{st[0], st[1], st[2]};
+    return FA_OK;
+}
+
+// Sizes of a call with N_q = Sq query rows and N_k = Sk key rows.  Returns
+// FA_OK, an error code, or 1 when there is nothing to compute.
+int check_sizes_qk(int B, int H, int Sq, int Sk, int d, float scale, int dtype) {
+    int rq = check_sizes(B, H, Sq, d, scale, dtype);
+    if (rq < 0) return rq;
+    int rk = check_sizes(B, H, Sk, d, scale, dtype);
+    if (rk < 0) return rk;
+    if ((long long)B * H == 0 || Sq == 0) return 1;
+    if (Sk == 0) return fail(FA_ERR_INVALID_ARG, "no key rows (Sk = 0) for %d query rows", Sq);
+    return FA_OK;
+}
+
 // ---- optional kernel timing (fa_profile_enable / fa_profile_read)
 enum { PROF_FWD = 0, PROF_PRE = 1, PROF_BWD = 2, PROF_CONV = 3, PROF_DQ = 4, PROF_KINDS = 5 };
 struct ProfRec { cudaEvent_t a, b; int kind; };
@@ -201,23 +236,49 @@ int fa_version(void) { return 100; }
 
 const char* fa_get_last_error(void) { return g_err; }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_common(const void* q, const long long* sq, const void* k, const long long* sk, const void* v,
+               const long long* sv, void* o, const long long* so, float* lse, int B, int H, int Sq, int Sk, int d,
+               int causal, float scale, int dtype, void* stream) {
     g_err[0] = 0;
-    int rc = check_sizes(B, H, S, d, scale, dtype);
+    int rc = check_sizes_qk(B, H, Sq, Sk, d, scale, dtype);
     if (rc == 1) return FA_OK;
     if (rc) return rc;
     if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
         (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")))
         return rc;
-    fa::FwdArgs a{q, k, v, o, lse, B, H, S, d, causal ? 1 : 0, scale, dtype,
+    fa::FwdArgs a{q, k, v, o, lse, B, H, Sq, d, causal ? 1 : 0, scale, dtype,
                   static_cast<cudaStream_t>(stream), nullptr};
+    a.Sk = Sk;
+    if ((rc = get_view(sq, B, H, Sq, d, dtype, "q", &a.vq)) || (rc = get_view(sk, B, H, Sk, d, dtype, "k", &a.vk)) ||
+        (rc = get_view(sv, B, H, Sk, d, dtype, "v", &a.vv)) || (rc = get_view(so, B, H, Sq, d, dtype, "o", &a.vo)))
+        return rc;
     if ((rc = status_ptr(&a.status))) return rc;
     cudaError_t e = timed(PROF_FWD, a.stream, [&] {
         return dtype == FA_BF16 ? fa::launch_fwd_tc(a) : fa::launch_fwd_simt(a);
     });
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
+    return fwd_common(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, B, H, S, S, d, causal, scale, dtype,
+                      stream);
+}
+
+int fa_fwd_strided(const void* q, const long long* q_strides, const void* k, const long long* k_strides,
+                   const void* v, const long long* v_strides, void* o, const long long* o_strides, float* lse,
+                   int B, int H, int Sq, int Sk, int d, int causal, float scale, int dtype, void* stream) {
+    return fwd_common(q, q_strides, k, k_strides, v, v_strides, o, o_strides, lse, B, H, Sq, Sk, d, causal, scale,
+                      dtype, stream);
 }
 
 int fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
@@ -236,6 +297,8 @@ int fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, f
         return fail(FA_ERR_UNSUPPORTED, "key_begin %d is not a multiple of 128", key_begin);
     fa::FwdArgs a{q, k, v, nullptr, lse_part, B, H, S, d, causal ? 1 : 0, scale, dtype,
                   static_cast<cudaStream_t>(stream), nullptr};
+    a.Sk = S;
+    a.vq = a.vk = a.vv = a.vo = fa::contiguous_view(H, S, d);
     if ((rc = status_ptr(&a.status))) return rc;
     cudaError_t e = timed(PROF_FWD, a.stream, [&] {
         return dtype == FA_BF16 ? fa::launch_fwd_tc_partial(a, key_begin, key_end, o_part)
@@ -271,31 +334,47 @@ size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype) {
 
 namespace {
 
-// fa_bwd and fa_bwd_deterministic: the same checks, D preprocess and dK/dV
-// loop; dQ either by atomics into dQacc plus a convert, or by its own
+// Every backward entry point: the same checks, D preprocess and dK/dV loop;
+// dQ either by atomics into dQacc plus a convert, or (det) by its own
 // query-tile-outer pass.
-int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dO,
-               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-               int B, int H, int S, int d, int causal, float scale, int dtype, void* stream, bool det) {
+int bwd_common(const void* q, const long long* sq, const void* k, const long long* sk, const void* v,
+               const long long* sv, const void* o, const long long* so, const void* dO, const long long* sdo,
+               const float* lse, void* dq, const long long* sdq, void* dk, const long long* sdk, void* dv,
+               const long long* sdv, void* workspace, size_t workspace_bytes, int B, int H, int Sq, int Sk, int d,
+               int causal, float scale, int dtype, void* stream, bool det) {
     g_err[0] = 0;
-    int rc = check_sizes(B, H, S, d, scale, dtype);
-    if (rc == 1) return FA_OK;
-    if (rc) return rc;
+    int rc = check_sizes_qk(B, H, Sq, Sk, d, scale, dtype);
+    const bool keys_only = rc == 1 && (long long)B * H > 0 && Sk > 0;   // no queries: dK = dV = 0
+    if (rc == 1 && !keys_only) return FA_OK;
+    if (rc < 0) return rc;
+    if ((rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv"))) return rc;
+    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, nullptr, nullptr, B, H, Sq, d, causal ? 1 : 0, scale,
+                  dtype, static_cast<cudaStream_t>(stream), nullptr};
+    a.Sk = Sk;
+    if ((rc = get_view(sdk, B, H, Sk, d, dtype, "dk", &a.vdk)) || (rc = get_view(sdv, B, H, Sk, d, dtype, "dv", &a.vdv)))
+        return rc;
+    if (keys_only) {
+        cudaError_t e = fa::launch_zero_rows(a, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "zero dk/dv launch");
+        return FA_OK;
+    }
     if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
         (rc = check_ptr(o, "o")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(lse, "lse")) ||
-        (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+        (rc = check_ptr(dq, "dq")))
         return rc;
-    const size_t rows = (size_t)B * H * S;
-    const size_t need = det ? rows * sizeof(float) : fa_bwd_workspace_size(B, H, S, d, dtype);
+    if ((rc = get_view(sq, B, H, Sq, d, dtype, "q", &a.vq)) || (rc = get_view(sk, B, H, Sk, d, dtype, "k", &a.vk)) ||
+        (rc = get_view(sv, B, H, Sk, d, dtype, "v", &a.vv)) || (rc = get_view(so, B, H, Sq, d, dtype, "o", &a.vo)) ||
+        (rc = get_view(sdo, B, H, Sq, d, dtype, "dO", &a.vdo)) || (rc = get_view(sdq, B, H, Sq, d, dtype, "dq", &a.vdq)))
+        return rc;
+    const size_t rows = (size_t)B * H * Sq;
+    const size_t need = det ? rows * sizeof(float) : fa_bwd_workspace_size(B, H, Sq, d, dtype);
     if (!workspace || workspace_bytes < need)
         return fail(FA_ERR_WORKSPACE, "workspace %p of %zu bytes, need %zu", workspace, workspace_bytes, need);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
-    float* Dvec = static_cast<float*>(workspace);
-    float* dQacc = det ? nullptr
-                       : reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * sizeof(float), 256));
-    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, Dvec, dQacc, B, H, S, d, causal ? 1 : 0, scale,
-                  dtype, static_cast<cudaStream_t>(stream), nullptr};
+    a.Dvec = static_cast<float*>(workspace);
+    a.dQacc = det ? nullptr
+                  : reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * sizeof(float), 256));
     if ((rc = status_ptr(&a.status))) return rc;
     cudaError_t e = timed(PROF_PRE, a.stream, [&] { return fa::launch_bwd_preprocess(a); });
     if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
@@ -304,6 +383,13 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
         return det ? fa::launch_bwd_tc_dkdv(a) : fa::launch_bwd_tc(a);
     });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    if (causal && dtype == FA_BF16) {
+        // The tensor-core kernel covers the key tiles some query reaches under
+        // the causal mask; the key rows of the tiles past the last query tile
+        // get zero gradients here.
+        e = fa::launch_zero_rows(a, ((Sq + 127) / 128) * 128);
+        if (e != cudaSuccess) return cuda_fail(e, "zero dk/dv launch");
+    }
     if (det) {
         e = timed(PROF_DQ, a.stream, [&] {
             return dtype == FA_BF16 ? fa::launch_bwd_dq_tc(a) : fa::launch_bwd_dq_simt(a);
@@ -324,16 +410,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv,
            void* workspace, size_t workspace_bytes,
            int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
-    return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, S, d, causal, scale,
-                      dtype, stream, false);
+    return bwd_common(q, nullptr, k, nullptr, v, nullptr, o, nullptr, dO, nullptr, lse, dq, nullptr, dk, nullptr, dv,
+                      nullptr, workspace, workspace_bytes, B, H, S, S, d, causal, scale, dtype, stream, false);
 }
 
 int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dO,
                          const float* lse, void* dq, void* dk, void* dv,
                          void* workspace, size_t workspace_bytes,
                          int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
-    return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, S, d, causal, scale,
-                      dtype, stream, true);
+    return bwd_common(q, nullptr, k, nullptr, v, nullptr, o, nullptr, dO, nullptr, lse, dq, nullptr, dk, nullptr, dv,
+                      nullptr, workspace, workspace_bytes, B, H, S, S, d, causal, scale, dtype, stream, true);
+}
+
+int fa_bwd_strided(const void* q, const long long* q_strides, const void* k, const long long* k_strides,
+                   const void* v, const long long* v_strides, const void* o, const long long* o_strides,
+                   const void* dO, const long long* do_strides, const float* lse,
+                   void* dq, const long long* dq_strides, void* dk, const long long* dk_strides,
+                   void* dv, const long long* dv_strides, void* workspace, size_t workspace_bytes,
+                   int B, int H, int Sq, int Sk, int d, int causal, float scale, int dtype, int deterministic,
+                   void* stream) {
+    return bwd_common(q, q_strides, k, k_strides, v, v_strides, o, o_strides, dO, do_strides, lse, dq, dq_strides,
+                      dk, dk_strides, dv, dv_strides, workspace, workspace_bytes, B, H, Sq, Sk, d, causal, scale,
+                      dtype, stream, deterministic != 0);
 }
 
 size_t fa_fwd_bwd_host_buffer_size(int B, int H, int S, int d, int dtype) {

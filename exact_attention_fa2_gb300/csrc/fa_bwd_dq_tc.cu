@@ -23,6 +23,8 @@
 // allocation and the S/dP issuer, warp 10 the dQ issuer.  One thread issues a
 // tcgen05.mma only every ~80 cycles, so two issuing threads keep the tensor
 // cores busier than one.
+// Shapes as in the key-tile-outer kernel: N_q queries, N_k keys, strided
+// [B, H, rows, d] views (strides multiples of 8 elements), contiguous L, D.
 // Tensor Memory columns: S [0,128), dP [128,256), two bf16 dS buffers
 // [256,320) and [320,384), dQ [384, 384+d).  S_{j+1} and dP_{j+1} are issued
 // as soon as the dS warps have read S_j and dP_j, so the products of the next
@@ -79,11 +81,14 @@ struct DqParams {
     CUtensorMap tk[2];
     CUtensorMap tv[2];
     CUtensorMap tdo[2];
-    const float* lse;
-    const float* Dvec;
+    const float* lse;     // contiguous [B*H, S]
+    const float* Dvec;    // contiguous [B*H, S]
     __nv_bfloat16* dq;
     unsigned int* status;
-    int S;
+    View vdq;             // element strides of dq
+    int H;
+    int S;                // query rows N_q
+    int Sk;               // key rows N_k
     int n_q;
     int n_kv;
     int causal;
@@ -126,6 +131,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
     const int BH = (int)(gridDim.x / (unsigned)p.n_q);
     const int rank = (int)blockIdx.x / BH;
     const int bh = (int)blockIdx.x - rank * BH;
+    const int bb = bh / p.H, hh = bh - bb * p.H;
     const int qt = p.causal ? (p.n_q - 1 - rank) : rank;
     const int S = p.S;
     const int nj = p.causal ? min(qt + 1, p.n_kv) : p.n_kv;   // key tiles at or below the diagonal
@@ -173,8 +179,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
             mbar_arrive_expect_tx(qd_full, 2 * G::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-                tma_load_3d(sb + G::Q_OFF + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64, qt * BQ, bh, qd_full);
-                tma_load_3d(sb + G::DO_OFF + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64, qt * BQ, bh, qd_full);
+                tma_load_4d(sb + G::Q_OFF + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64, qt * BQ, hh, bb,
+                            qd_full);
+                tma_load_4d(sb + G::DO_OFF + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64, qt * BQ, hh, bb,
+                            qd_full);
             }
             for (int j = 0; j < nj; ++j) {
                 const int st = j % NS;
@@ -184,11 +192,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
                 mbar_arrive_expect_tx(k_full(st), G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(kdst + C::tile_off(c, BK), &p.tk[C::map_index(c)], c * 64, j * BK, bh, k_full(st));
+                    tma_load_4d(kdst + C::tile_off(c, BK), &p.tk[C::map_index(c)], c * 64, j * BK, hh, bb, k_full(st));
                 mbar_arrive_expect_tx(v_full(st), G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(kdst + G::TILE + C::tile_off(c, BK), &p.tv[C::map_index(c)], c * 64, j * BK, bh,
+                    tma_load_4d(kdst + G::TILE + C::tile_off(c, BK), &p.tv[C::map_index(c)], c * 64, j * BK, hh, bb,
                                 v_full(st));
                 issued = j + 1;
             }
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
         const float l2 = row < S ? p.lse[grow] * FA_LOG2E : INFINITY;   // P = 0 on rows past S
         const float dd = row < S ? p.Dvec[grow] : 0.f;
         const float c = p.c;
-        const int key_lim = p.causal ? min(row, S - 1) : S - 1;
+        const int key_lim = p.causal ? min(row, p.Sk - 1) : p.Sk - 1;
         bool ok = true;
         for (int j = 0; j < nj; ++j) {
             if (!(ok = warp_wait(s_full, j & 1, abort, p.status))) break;
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
             mbar_arrive(s_free);                       // S, dP columns may take the next key tile
             const int kbase = j * BK + 64 * h;
             // Only the diagonal tile and a ragged last tile need the per-key mask.
-            const bool masked = (p.causal && j == qt) || ((j + 1) * BK > S);
+            const bool masked = (p.causal && j == qt) || ((j + 1) * BK > p.Sk);
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
                 for (int e = 0; e < 8; ++e)
                     v[e] = pack_bf16(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
                 if (row < S) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + 16 * u);
+                    uint4* dst = reinterpret_cast<uint4*>(p.dq + p.vdq.off(bb, hh, row) + 16 * u);
                     dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
                     dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
                 }
@@ -356,20 +364,28 @@ cudaError_t bwd_dq_tc_launch(const BwdArgs& a) {
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
     const void* src[4] = {a.q, a.k, a.v, a.dO};
+    const int rows[4] = {a.S, a.Sk, a.Sk, a.S};
+    const View views[4] = {a.vq, a.vk, a.vv, a.vdo};
     CUtensorMap* maps[4] = {p.tq, p.tk, p.tv, p.tdo};
     for (int i = 0; i < 4; ++i) {
         cudaError_t e;
-        if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, 128)) != cudaSuccess) return e;
-        if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess)
+        if (C::N64 > 0 &&
+            (e = make_tmap_bf16_4d(&maps[i][0], src[i], D, rows[i], a.H, a.B, views[i], 64, 128)) != cudaSuccess)
+            return e;
+        if (C::REM > 0 && !C::PAD &&
+            (e = make_tmap_bf16_4d(&maps[i][1], src[i], D, rows[i], a.H, a.B, views[i], C::REM, 128)) != cudaSuccess)
             return e;
     }
     p.lse = a.lse;
     p.Dvec = a.Dvec;
     p.dq = static_cast<__nv_bfloat16*>(a.dq);
     p.status = a.status;
+    p.vdq = a.vdq;
+    p.H = a.H;
     p.S = a.S;
+    p.Sk = a.Sk;
     p.n_q = (a.S + BQ - 1) / BQ;
-    p.n_kv = (a.S + BK - 1) / BK;
+    p.n_kv = (a.Sk + BK - 1) / BK;
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;

@@ -26,6 +26,10 @@
 // and the single-thread MMA issuer.
 // Tensor Memory columns: dV [0,128), dK [128,256), S^T/P^T [256,384),
 // dP^T [384,512), which dQ_i reuses once dS^T has been formed.
+// Shapes: N_q queries and N_k keys (Algorithm 2's Q in R^{N_q x d}, K, V in
+// R^{N_k x d}), causal keeping key j for query i when j <= i; every
+// [B, H, rows, d] operand is a view with strides that are multiples of 8
+// elements (4-D TMA maps); L, D and the dQ accumulator are contiguous.
 
 #include "fa_common.cuh"
 #include "fa_launch.h"
@@ -116,12 +120,16 @@ struct BwdParams {
     CUtensorMap tv[2];
     CUtensorMap tdo[2];
     CUtensorMap tdq[2];
-    const float* lse;
-    const float* Dvec;
+    const float* lse;     // contiguous [B*H, S]
+    const float* Dvec;    // contiguous [B*H, S]
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     unsigned int* status;
-    int S;
+    View vdk, vdv;        // element strides of dk, dv
+    uint32_t map3;        // bit i: map i of (q, k, v, dO) is 3-D over (col, row, b*H + h)
+    int H;
+    int S;                // query rows N_q
+    int Sk;               // key rows N_k
     int n_q;
     int n_kv;
     int causal;
@@ -186,10 +194,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const int BH = (int)(gridDim.x / (unsigned)p.n_kv);
     const int j = (int)blockIdx.x / BH;
     const int bh = (int)blockIdx.x - j * BH;
+    const int bb = bh / p.H, hh = bh - bb * p.H;
     const int S = p.S;
     const int k0 = j * BK;
     const int i0 = p.causal ? j : 0;          // query tiles above the diagonal are fully masked
-    const int n_it = p.n_q - i0;
+    const int n_it = p.n_q - i0;              // >= 1: the grid holds no key tile past the last query tile
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -237,8 +246,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             mbar_arrive_expect_tx(kv_full, 2 * G::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-                tma_load_3d(sb + G::K_OFF + C::tile_off(c, BK), &p.tk[C::map_index(c)], c * 64, k0, bh, kv_full);
-                tma_load_3d(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], c * 64, k0, bh, kv_full);
+                tma_load_view(sb + G::K_OFF + C::tile_off(c, BK), &p.tk[C::map_index(c)], p.map3 & 2u, c * 64, k0, hh,
+                              bb, bh, kv_full);
+                tma_load_view(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], p.map3 & 4u, c * 64, k0, hh,
+                              bb, bh, kv_full);
             }
         }
         const size_t rb = (size_t)bh * S;
@@ -263,8 +274,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mbar_arrive_expect_tx(q_full(s), 2 * G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_3d(q_slot(s) + C::tile_off(c, BQ), &p.tq[C::map_index(c)], c * 64, q0, bh, q_full(s));
-                    tma_load_3d(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], c * 64, q0, bh, q_full(s));
+                    tma_load_view(q_slot(s) + C::tile_off(c, BQ), &p.tq[C::map_index(c)], p.map3 & 1u, c * 64, q0, hh,
+                                  bb, bh, q_full(s));
+                    tma_load_view(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], p.map3 & 8u, c * 64, q0, hh,
+                                  bb, bh, q_full(s));
                 }
             }
 #pragma unroll
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const int wq = warp & 3;
         const int jr = wq * 32 + lane;                 // key row inside the tile
         const int key = k0 + jr;
-        const bool key_ok = key < S;
+        const bool key_ok = key < p.Sk;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + TM_S;
         const uint32_t tP = tmem + lane_off + TM_DP;
@@ -480,7 +493,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         // dK, dV rows of this key tile (16-column units split between the halves).
         if (ok && warp_wait(done, 0, abort, p.status)) {
             tc_fence_after();
-            const size_t row = (size_t)bh * S + key;
 #pragma unroll
             for (int u = h; u < D / 16; u += 2) {
                 uint32_t a[16], b[16];
@@ -496,8 +508,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     vb[e] = pack_bf16(__uint_as_float(b[2 * e]) * p.scale, __uint_as_float(b[2 * e + 1]) * p.scale);
                 }
                 if (key_ok) {
-                    uint4* dvp = reinterpret_cast<uint4*>(p.dv + row * D + 16 * u);
-                    uint4* dkp = reinterpret_cast<uint4*>(p.dk + row * D + 16 * u);
+                    uint4* dvp = reinterpret_cast<uint4*>(p.dv + p.vdv.off(bb, hh, key) + 16 * u);
+                    uint4* dkp = reinterpret_cast<uint4*>(p.dk + p.vdk.off(bb, hh, key) + 16 * u);
                     dvp[0] = make_uint4(va[0], va[1], va[2], va[3]);
                     dvp[1] = make_uint4(va[4], va[5], va[6], va[7]);
                     dkp[0] = make_uint4(vb[0], vb[1], vb[2], vb[3]);
@@ -583,12 +595,20 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
     const void* src[4] = {a.q, a.k, a.v, a.dO};
+    const int rows[4] = {a.S, a.Sk, a.Sk, a.S};
+    const View views[4] = {a.vq, a.vk, a.vv, a.vdo};
     CUtensorMap* maps[4] = {p.tq, p.tk, p.tv, p.tdo};
     for (int i = 0; i < 4; ++i) {
         cudaError_t e;
-        if (C::N64 > 0 && (e = make_tmap_bf16_3d(&maps[i][0], src[i], D, a.S, BH, 64, 128)) != cudaSuccess) return e;
-        if (C::REM > 0 && !C::PAD && (e = make_tmap_bf16_3d(&maps[i][1], src[i], D, a.S, BH, C::REM, 128)) != cudaSuccess)
+        bool r3 = false;
+        if (C::N64 > 0 &&
+            (e = make_tmap_bf16_view(&maps[i][0], &r3, src[i], D, rows[i], a.H, a.B, views[i], 64, 128)) != cudaSuccess)
             return e;
+        if (C::REM > 0 && !C::PAD &&
+            (e = make_tmap_bf16_view(&maps[i][1], &r3, src[i], D, rows[i], a.H, a.B, views[i], C::REM, 128)) !=
+                cudaSuccess)
+            return e;
+        if (r3) p.map3 |= 1u << i;
     }
     if (WITH_DQ) {
         using QC = DqChunks<D>;
@@ -601,9 +621,16 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.status = a.status;
+    p.vdk = a.vdk;
+    p.vdv = a.vdv;
+    p.H = a.H;
     p.S = a.S;
+    p.Sk = a.Sk;
     p.n_q = (a.S + BQ - 1) / BQ;
-    p.n_kv = (a.S + BK - 1) / BK;
+    p.n_kv = (a.Sk + BK - 1) / BK;
+    // Causal: key tiles past the last query tile are attended by no query;
+    // their zero gradients are written by a separate launch.
+    if (a.causal) p.n_kv = std::min(p.n_kv, p.n_q);
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;

@@ -32,6 +32,11 @@
 // rounding of P (letting the max lag by a few binades doubles the bf16 error of
 // O for sharp softmax rows).  A warp rescales its rows of O only when one of
 // its rows' max grew.  Fully masked causal tiles are never loaded or multiplied.
+//
+// Shapes: N_q query rows and N_k key rows may differ (Algorithm 1 takes Q in
+// R^{N_q x d}, K, V in R^{N_k x d}); the causal mask keeps key j for query i
+// when j <= i.  Q, K, V and O are [B, H, rows, d] views with any strides that
+// are multiples of 8 elements (the TMA maps are 4-D over b, h, row, col).
 
 #include "fa_common.cuh"
 #include "fa_launch.h"
@@ -89,10 +94,12 @@ struct FwdParams {
     CUtensorMap tk[2];
     CUtensorMap tv[2];
     __nv_bfloat16* o;
-    float* o32;       // partial attention: fp32 output (o unused)
-    float* lse;
+    float* o32;       // partial attention: contiguous fp32 output (o unused)
+    float* lse;       // contiguous [B*H, S]
     unsigned int* status;
-    int S;            // query rows (and the row pitch of every array)
+    View vo;          // element strides of o
+    int H;
+    int S;            // query rows
     int n_units;      // 256-row query blocks per head
     int Sk;           // key rows seen by the K/V tensor maps
     int n_kv;         // 128-key tiles in [0, Sk)
@@ -153,6 +160,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     const int BH = (int)(gridDim.x / (unsigned)p.n_units);
     const int rank = (int)blockIdx.x / BH;
     const int bh = (int)blockIdx.x - rank * BH;
+    const int bb = bh / p.H, hh = bh - bb * p.H;
     const int unit = p.causal ? (p.n_units - 1 - rank) : rank;
     const int S = p.S;
     const int qtA = 2 * unit;
@@ -209,10 +217,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             mbar_arrive_expect_tx(q_full, (hasB ? 2 : 1) * G::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-                tma_load_3d(sb + G::QA_OFF + C::tile_off(c, BM), &p.tq[C::map_index(c)], c * 64, qtA * BM, bh, q_full);
+                tma_load_4d(sb + G::QA_OFF + C::tile_off(c, BM), &p.tq[C::map_index(c)], c * 64, qtA * BM, hh, bb,
+                            q_full);
                 if (hasB)
-                    tma_load_3d(sb + G::QB_OFF + C::tile_off(c, BM), &p.tq[C::map_index(c)], c * 64, (qtA + 1) * BM,
-                                bh, q_full);
+                    tma_load_4d(sb + G::QB_OFF + C::tile_off(c, BM), &p.tq[C::map_index(c)], c * 64, (qtA + 1) * BM,
+                                hh, bb, q_full);
             }
             for (int j = 0; j <= jB; ++j) {
                 const int st = j % NS;
@@ -221,15 +230,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
                 mbar_arrive_expect_tx(k_full(st), G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sb + G::K_OFF + st * G::TILE + C::tile_off(c, BN), &p.tk[C::map_index(c)],
-                                c * 64, j * BN, bh, k_full(st));
+                    tma_load_4d(sb + G::K_OFF + st * G::TILE + C::tile_off(c, BN), &p.tk[C::map_index(c)],
+                                c * 64, j * BN, hh, bb, k_full(st));
                 issued_k = j + 1;
                 if (!mbar_wait(v_empty(st), ph ^ 1, abort, p.status, WAIT_LIMIT_NS)) break;
                 mbar_arrive_expect_tx(v_full(st), G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_3d(sb + G::V_OFF + st * G::TILE + C::tile_off(c, BN), &p.tv[C::map_index(c)],
-                                c * 64, j * BN, bh, v_full(st));
+                    tma_load_4d(sb + G::V_OFF + st * G::TILE + C::tile_off(c, BN), &p.tv[C::map_index(c)],
+                                c * 64, j * BN, hh, bb, v_full(st));
                 issued_v = j + 1;
             }
             if (*abort) {
@@ -504,7 +513,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)bh * S + row) * D + 16 * u);
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + p.vo.off(bb, hh, row) + 16 * u);
                     dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
@@ -526,24 +535,29 @@ cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o
     FwdParams p;
     memset(&p, 0, sizeof(p));
     const int BH = a.B * a.H;
-    // K and V tensor maps start at the key window; rows keep the pitch of S.
+    // K and V tensor maps start at the key window [key_begin, key_end) of the
+    // a.Sk keys; the views' strides are unchanged.
     const int Sk = key_end - key_begin;
-    const size_t koff = (size_t)key_begin * D * 2;
-    const void* src[3] = {a.q, static_cast<const char*>(a.k) + koff, static_cast<const char*>(a.v) + koff};
+    const void* src[3] = {a.q, static_cast<const __nv_bfloat16*>(a.k) + (size_t)key_begin * a.vk.s,
+                          static_cast<const __nv_bfloat16*>(a.v) + (size_t)key_begin * a.vv.s};
     const int rows[3] = {a.S, Sk, Sk};
+    const View views[3] = {a.vq, a.vk, a.vv};
     CUtensorMap* maps[3] = {p.tq, p.tk, p.tv};
     for (int i = 0; i < 3; ++i) {
         cudaError_t e;
-        if (C::N64 > 0 && (e = make_tmap_bf16_3d_rows(&maps[i][0], src[i], D, rows[i], a.S, BH, 64, BM)) != cudaSuccess)
+        if (C::N64 > 0 &&
+            (e = make_tmap_bf16_4d(&maps[i][0], src[i], D, rows[i], a.H, a.B, views[i], 64, BM)) != cudaSuccess)
             return e;
         if (C::REM > 0 && !C::PAD &&
-            (e = make_tmap_bf16_3d_rows(&maps[i][1], src[i], D, rows[i], a.S, BH, C::REM, BM)) != cudaSuccess)
+            (e = make_tmap_bf16_4d(&maps[i][1], src[i], D, rows[i], a.H, a.B, views[i], C::REM, BM)) != cudaSuccess)
             return e;
     }
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.o32 = o32;
     p.lse = a.lse;
     p.status = a.status;
+    p.vo = a.vo;
+    p.H = a.H;
     p.S = a.S;
     p.n_units = (a.S + 2 * BM - 1) / (2 * BM);
     p.Sk = Sk;
@@ -563,12 +577,12 @@ cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
     switch (a.d) {
-        case 16: return fwd_tc_launch<16, false>(a, 0, a.S, nullptr);
-        case 32: return fwd_tc_launch<32, false>(a, 0, a.S, nullptr);
-        case 64: return fwd_tc_launch<64, false>(a, 0, a.S, nullptr);
-        case 80: return fwd_tc_launch<80, false>(a, 0, a.S, nullptr);
-        case 96: return fwd_tc_launch<96, false>(a, 0, a.S, nullptr);
-        case 128: return fwd_tc_launch<128, false>(a, 0, a.S, nullptr);
+        case 16: return fwd_tc_launch<16, false>(a, 0, a.Sk, nullptr);
+        case 32: return fwd_tc_launch<32, false>(a, 0, a.Sk, nullptr);
+        case 64: return fwd_tc_launch<64, false>(a, 0, a.Sk, nullptr);
+        case 80: return fwd_tc_launch<80, false>(a, 0, a.Sk, nullptr);
+        case 96: return fwd_tc_launch<96, false>(a, 0, a.Sk, nullptr);
+        case 128: return fwd_tc_launch<128, false>(a, 0, a.Sk, nullptr);
         default: return cudaErrorInvalidValue;
     }
 }

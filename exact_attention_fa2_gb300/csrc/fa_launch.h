@@ -10,18 +10,30 @@ namespace fa {
 
 enum { DT_BF16 = 0, DT_FP32 = 1 };
 
+// Element strides of a [B, H, rows, d] view whose head dimension is
+// contiguous (stride 1).
+struct View {
+    long long b, h, s;
+    __host__ __device__ long long off(int bi, int hi, long long row) const { return bi * b + hi * h + row * s; }
+};
+inline View contiguous_view(int H, int rows, int d) {
+    return View{(long long)H * rows * d, (long long)rows * d, (long long)d};
+}
+
 struct FwdArgs {
     const void* q;
     const void* k;
     const void* v;
     void* o;
-    float* lse;
-    int B, H, S, d;
+    float* lse;             // contiguous [B, H, S] fp32
+    int B, H, S, d;         // S = N_q, the number of query rows
     int causal;
     float scale;
     int dtype;
     cudaStream_t stream;
     unsigned int* status;   // device status word (timeouts, index checks)
+    int Sk;                 // N_k, the number of key rows
+    View vq, vk, vv, vo;    // strides of q, o ([B,H,S,d]) and k, v ([B,H,Sk,d])
 };
 
 struct BwdArgs {
@@ -36,12 +48,14 @@ struct BwdArgs {
     void* dv;
     float* Dvec;            // [B*H*S] fp32, inside the workspace
     float* dQacc;           // [B*H*S*d] fp32, inside the workspace (null: deterministic backward)
-    int B, H, S, d;
+    int B, H, S, d;         // S = N_q
     int causal;
     float scale;
     int dtype;
     cudaStream_t stream;
     unsigned int* status;
+    int Sk;                 // N_k
+    View vq, vk, vv, vo, vdo, vdq, vdk, vdv;   // q, o, dO, dq: [B,H,S,d]; k, v, dk, dv: [B,H,Sk,d]
 };
 
 // Launch `kern` as a programmatic dependent of the previous kernel on the
@@ -71,6 +85,9 @@ cudaError_t launch_bwd_simt(const BwdArgs& a);
 // Backward helpers: D = rowsum(O*dO) plus zeroing of dQacc; dQacc -> dq.
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_dq_convert(const BwdArgs& a);
+// dK = dV = 0 on key rows [row0, Sk): keys no query attends (no query rows
+// at all, or causal keys past the last query tile).
+cudaError_t launch_zero_rows(const BwdArgs& a, int row0);
 
 // Record `msg` as the calling thread's last error (read by fa_get_last_error)
 // and return `code`.

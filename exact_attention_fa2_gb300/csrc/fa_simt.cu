@@ -28,10 +28,11 @@ constexpr int BK = 64;
 constexpr int NT = 256;
 constexpr int LDP = BK + 1;
 
-// Load rows [row0, row0+64) of one contiguous [S, D] slice into shared memory
-// as fp32 with leading dimension ld; rows at or beyond S are zero.
+// Load rows [row0, row0+64) of one [rows, D] slice (row stride rs elements,
+// 16-byte aligned rows) into shared memory as fp32 with leading dimension ld;
+// rows at or beyond S are zero.
 template <typename T, int D>
-__device__ __forceinline__ void load_tile(float* dst, int ld, const T* src, int row0, int S) {
+__device__ __forceinline__ void load_tile(float* dst, int ld, const T* src, long long rs, int row0, int S) {
     constexpr int VN = Vec16<T>::N;
     constexpr int CPR = D / VN;
     for (int idx = threadIdx.x; idx < 64 * CPR; idx += NT) {
@@ -39,7 +40,7 @@ __device__ __forceinline__ void load_tile(float* dst, int ld, const T* src, int 
         const int c = (idx % CPR) * VN;
         float tmp[VN];
         if (row0 + r < S) {
-            Vec16<T>::load(src + (size_t)(row0 + r) * D + c, tmp);
+            Vec16<T>::load(src + (row0 + r) * rs + c, tmp);
         } else {
 #pragma unroll
             for (int i = 0; i < VN; ++i) tmp[i] = 0.f;
@@ -61,9 +62,9 @@ constexpr size_t bwd_smem_bytes() {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(NT)
-fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                T* __restrict__ o, float* __restrict__ lse, int S, int n_qtiles, int causal,
-                float scale_log2, int kb, int ke) {
+fwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View vk, const T* __restrict__ v,
+                View vv, T* __restrict__ o, View vo, float* __restrict__ lse, int S, int H, int n_qtiles,
+                int causal, float scale_log2, int kb, int ke) {
     // Keys [kb, ke) only (the whole row for the plain forward); a row with no
     // admissible key gets O = 0 and L = -inf (partial attention).
     extern __shared__ float smem[];
@@ -81,9 +82,12 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     const int ty = tid / 16, tx = tid % 16;
     const int qt = n_qtiles - 1 - (int)blockIdx.x;   // long causal rows start first
     const int q0 = qt * BQ;
-    const size_t base = (size_t)blockIdx.y * S * D;
+    const int bb = (int)blockIdx.y / H, hh = (int)blockIdx.y - bb * H;
+    const T* qb = q + vq.off(bb, hh, 0);
+    const T* kbp = k + vk.off(bb, hh, 0);
+    const T* vbp = v + vv.off(bb, hh, 0);
 
-    load_tile<T, D>(Qs, LDQ, q + base, q0, S);
+    load_tile<T, D>(Qs, LDQ, qb, vq.s, q0, S);
     if (tid < 64) { m_s[tid] = -INFINITY; l_s[tid] = 0.f; }
 
     float acc[4][NC];
@@ -97,8 +101,8 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 
     for (int kt = 0; kt < n_k; ++kt) {
         __syncthreads();
-        load_tile<T, D>(Ks, LDK, k + base, kb + kt * BK, ke);
-        load_tile<T, D>(Vs, LDV, v + base, kb + kt * BK, ke);
+        load_tile<T, D>(Ks, LDK, kbp, vk.s, kb + kt * BK, ke);
+        load_tile<T, D>(Vs, LDV, vbp, vv.s, kb + kt * BK, ke);
         __syncthreads();
 
         // S tile (Algorithm 1 line 9), rows ty*4+r, columns tx+16c.
@@ -193,7 +197,7 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
             const float inv = l_s[lr] > 0.f ? 1.f / l_s[lr] : 0.f;
 #pragma unroll
             for (int c = 0; c < NC; ++c)
-                o[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(acc[r][c] * inv);
+                o[vo.off(bb, hh, row) + tx + 16 * c] = from_f32<T>(acc[r][c] * inv);
         }
     }
     if (tid < 64 && q0 + tid < S)
@@ -202,11 +206,11 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 
 template <typename T, int D>
 __global__ void __launch_bounds__(NT)
-bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                const T* __restrict__ dO, const float* __restrict__ lse,
+bwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View vk, const T* __restrict__ v,
+                View vv, const T* __restrict__ dO, View vdo, const float* __restrict__ lse,
                 const float* __restrict__ Dvec, float* __restrict__ dQacc,
-                T* __restrict__ dk, T* __restrict__ dv, int S, int causal, float scale,
-                float scale_log2) {
+                T* __restrict__ dk, View vdk, T* __restrict__ dv, View vdv, int S, int Sk, int H, int causal,
+                float scale, float scale_log2) {
     extern __shared__ float smem[];
     constexpr int LD = D + 1;
     constexpr int NC = D / 16;
@@ -224,10 +228,13 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     const int kt = blockIdx.x;            // early key tiles see the most query tiles
     const int k0 = kt * BK;
     const size_t bh = blockIdx.y;
-    const size_t base = bh * S * D;
+    const int bb = (int)bh / H, hh = (int)bh - bb * H;
+    const size_t base = bh * S * D;       // of the contiguous dQ accumulator
+    const T* qb = q + vq.off(bb, hh, 0);
+    const T* dob = dO + vdo.off(bb, hh, 0);
 
-    load_tile<T, D>(Ks, LD, k + base, k0, S);
-    load_tile<T, D>(Vs, LD, v + base, k0, S);
+    load_tile<T, D>(Ks, LD, k + vk.off(bb, hh, 0), vk.s, k0, Sk);
+    load_tile<T, D>(Vs, LD, v + vv.off(bb, hh, 0), vv.s, k0, Sk);
 
     float dk_acc[4][NC], dv_acc[4][NC];
 #pragma unroll
@@ -239,8 +246,8 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     for (int qt = causal ? kt : 0; qt < n_q; ++qt) {
         const int q0 = qt * BQ;
         __syncthreads();
-        load_tile<T, D>(Qs, LD, q + base, q0, S);
-        load_tile<T, D>(dOs, LD, dO + base, q0, S);
+        load_tile<T, D>(Qs, LD, qb, vq.s, q0, S);
+        load_tile<T, D>(dOs, LD, dob, vdo.s, q0, S);
         if (tid < 64) {
             const int row = q0 + tid;
             L2s[tid] = row < S ? lse[bh * S + row] * FA_LOG2E : INFINITY;
@@ -277,7 +284,7 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int col = k0 + tx + 16 * c;
-                const bool keep = col < S && row < S && (!causal || col <= row);
+                const bool keep = col < Sk && row < S && (!causal || col <= row);
                 const float p = keep ? exp2f(fmaf(s[r][c], scale_log2, -L2s[lr])) : 0.f;
                 const float ds = p * (dp[r][c] - Ds[lr]);
                 Ps[lr * LDP + tx + 16 * c] = round_to<T>(p);
@@ -338,11 +345,11 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int row = k0 + ty * 4 + r;
-        if (row < S) {
+        if (row < Sk) {
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                dk[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(dk_acc[r][c] * scale);
-                dv[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(dv_acc[r][c]);
+                dk[vdk.off(bb, hh, row) + tx + 16 * c] = from_f32<T>(dk_acc[r][c] * scale);
+                dv[vdv.off(bb, hh, row) + tx + 16 * c] = from_f32<T>(dv_acc[r][c]);
             }
         }
     }
@@ -354,9 +361,10 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 // order, so every dQ element has one fixed summation order and no atomics.
 template <typename T, int D>
 __global__ void __launch_bounds__(NT)
-bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                   const T* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ Dvec,
-                   T* __restrict__ dq, int S, int causal, float scale, float scale_log2) {
+bwd_dq_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View vk, const T* __restrict__ v,
+                   View vv, const T* __restrict__ dO, View vdo, const float* __restrict__ lse,
+                   const float* __restrict__ Dvec, T* __restrict__ dq, View vdq, int S, int Sk, int H, int causal,
+                   float scale, float scale_log2) {
     extern __shared__ float smem[];
     constexpr int LD = D + 1;
     constexpr int NC = D / 16;
@@ -374,10 +382,12 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     const int qt = causal ? n_q - 1 - (int)blockIdx.x : (int)blockIdx.x;   // longest rows first
     const int q0 = qt * BQ;
     const size_t bh = blockIdx.y;
-    const size_t base = bh * S * D;
+    const int bb = (int)bh / H, hh = (int)bh - bb * H;
+    const T* kb_ = k + vk.off(bb, hh, 0);
+    const T* vb_ = v + vv.off(bb, hh, 0);
 
-    load_tile<T, D>(Qs, LD, q + base, q0, S);
-    load_tile<T, D>(dOs, LD, dO + base, q0, S);
+    load_tile<T, D>(Qs, LD, q + vq.off(bb, hh, 0), vq.s, q0, S);
+    load_tile<T, D>(dOs, LD, dO + vdo.off(bb, hh, 0), vdo.s, q0, S);
     if (tid < 64) {
         const int row = q0 + tid;
         L2s[tid] = row < S ? lse[bh * S + row] * FA_LOG2E : INFINITY;
@@ -389,12 +399,13 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
 
-    const int n_k = causal ? qt + 1 : (S + BK - 1) / BK;
+    const int n_kall = (Sk + BK - 1) / BK;
+    const int n_k = causal ? min(qt + 1, n_kall) : n_kall;
     for (int kt = 0; kt < n_k; ++kt) {
         const int k0 = kt * BK;
         __syncthreads();
-        load_tile<T, D>(Ks, LD, k + base, k0, S);
-        load_tile<T, D>(Vs, LD, v + base, k0, S);
+        load_tile<T, D>(Ks, LD, kb_, vk.s, k0, Sk);
+        load_tile<T, D>(Vs, LD, vb_, vv.s, k0, Sk);
         __syncthreads();
         // S, dP (Eq. 13, 16): rows queries ty*4+r, columns keys tx+16c.
         float s[4][4], dp[4][4];
@@ -425,7 +436,7 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int col = k0 + tx + 16 * c;
-                const bool keep = col < S && row < S && (!causal || col <= row);
+                const bool keep = col < Sk && row < S && (!causal || col <= row);
                 const float pr = keep ? exp2f(fmaf(s[r][c], scale_log2, -L2s[lr])) : 0.f;
                 dSs[lr * LDP + tx + 16 * c] = round_to<T>(pr * (dp[r][c] - Ds[lr]));
             }
@@ -450,21 +461,21 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         const int row = q0 + ty * 4 + r;
         if (row < S) {
 #pragma unroll
-            for (int c = 0; c < NC; ++c) dq[base + (size_t)row * D + tx + 16 * c] = from_f32<T>(acc[r][c] * scale);
+            for (int c = 0; c < NC; ++c) dq[vdq.off(bb, hh, row) + tx + 16 * c] = from_f32<T>(acc[r][c] * scale);
         }
     }
 }
 
 template <typename T, int D>
-cudaError_t fwd_simt_launch(const FwdArgs& a, int kb, int ke, T* o) {
+cudaError_t fwd_simt_launch(const FwdArgs& a, int kb, int ke, T* o, View vo) {
     constexpr size_t smem = fwd_smem_bytes<D>();
     auto kern = fwd_simt_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int n_qtiles = (a.S + BQ - 1) / BQ;
     dim3 grid(n_qtiles, a.B * a.H);
-    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, o, a.lse,
-                                       a.S, n_qtiles, a.causal, a.scale * FA_LOG2E, kb, ke);
+    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, a.vq, (const T*)a.k, a.vk, (const T*)a.v, a.vv, o, vo,
+                                       a.lse, a.S, a.H, n_qtiles, a.causal, a.scale * FA_LOG2E, kb, ke);
     return cudaGetLastError();
 }
 
@@ -474,10 +485,10 @@ cudaError_t bwd_simt_launch(const BwdArgs& a) {
     auto kern = bwd_simt_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.S + BK - 1) / BK, a.B * a.H);
-    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.dO,
-                                       a.lse, a.Dvec, a.dQacc, (T*)a.dk, (T*)a.dv, a.S, a.causal,
-                                       a.scale, a.scale * FA_LOG2E);
+    dim3 grid((a.Sk + BK - 1) / BK, a.B * a.H);
+    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, a.vq, (const T*)a.k, a.vk, (const T*)a.v, a.vv,
+                                       (const T*)a.dO, a.vdo, a.lse, a.Dvec, a.dQacc, (T*)a.dk, a.vdk, (T*)a.dv,
+                                       a.vdv, a.S, a.Sk, a.H, a.causal, a.scale, a.scale * FA_LOG2E);
     return cudaGetLastError();
 }
 
@@ -488,8 +499,9 @@ cudaError_t bwd_dq_simt_launch(const BwdArgs& a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.S + BQ - 1) / BQ, a.B * a.H);
-    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, (const T*)a.k, (const T*)a.v, (const T*)a.dO, a.lse,
-                                       a.Dvec, (T*)a.dq, a.S, a.causal, a.scale, a.scale * FA_LOG2E);
+    kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, a.vq, (const T*)a.k, a.vk, (const T*)a.v, a.vv,
+                                       (const T*)a.dO, a.vdo, a.lse, a.Dvec, (T*)a.dq, a.vdq, a.S, a.Sk, a.H,
+                                       a.causal, a.scale, a.scale * FA_LOG2E);
     return cudaGetLastError();
 }
 
@@ -507,14 +519,14 @@ cudaError_t bwd_dq_simt_dispatch(const BwdArgs& a) {
 }
 
 template <typename T>
-cudaError_t fwd_simt_dispatch(const FwdArgs& a, int kb, int ke, T* o) {
+cudaError_t fwd_simt_dispatch(const FwdArgs& a, int kb, int ke, T* o, View vo) {
     switch (a.d) {
-        case 16: return fwd_simt_launch<T, 16>(a, kb, ke, o);
-        case 32: return fwd_simt_launch<T, 32>(a, kb, ke, o);
-        case 64: return fwd_simt_launch<T, 64>(a, kb, ke, o);
-        case 80: return fwd_simt_launch<T, 80>(a, kb, ke, o);
-        case 96: return fwd_simt_launch<T, 96>(a, kb, ke, o);
-        case 128: return fwd_simt_launch<T, 128>(a, kb, ke, o);
+        case 16: return fwd_simt_launch<T, 16>(a, kb, ke, o, vo);
+        case 32: return fwd_simt_launch<T, 32>(a, kb, ke, o, vo);
+        case 64: return fwd_simt_launch<T, 64>(a, kb, ke, o, vo);
+        case 80: return fwd_simt_launch<T, 80>(a, kb, ke, o, vo);
+        case 96: return fwd_simt_launch<T, 96>(a, kb, ke, o, vo);
+        case 128: return fwd_simt_launch<T, 128>(a, kb, ke, o, vo);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -535,14 +547,14 @@ cudaError_t bwd_simt_dispatch(const BwdArgs& a) {
 }  // namespace
 
 cudaError_t launch_fwd_simt(const FwdArgs& a) {
-    return a.dtype == DT_FP32 ? fwd_simt_dispatch<float>(a, 0, a.S, (float*)a.o)
-                              : fwd_simt_dispatch<__nv_bfloat16>(a, 0, a.S, (__nv_bfloat16*)a.o);
+    return a.dtype == DT_FP32 ? fwd_simt_dispatch<float>(a, 0, a.Sk, (float*)a.o, a.vo)
+                              : fwd_simt_dispatch<__nv_bfloat16>(a, 0, a.Sk, (__nv_bfloat16*)a.o, a.vo);
 }
 
 cudaError_t launch_fwd_simt_partial(const FwdArgs& a, int key_begin, int key_end, float* o32) {
     // fp32 storage only: the partial output is fp32 like the inputs.
     if (a.dtype != DT_FP32) return cudaErrorInvalidValue;
-    return fwd_simt_dispatch<float>(a, key_begin, key_end, o32);
+    return fwd_simt_dispatch<float>(a, key_begin, key_end, o32, contiguous_view(a.H, a.S, a.d));
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a) {

@@ -98,6 +98,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
         : "memory");
 }
 
+// 4-D tiled load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// Load of one box of a [B, H, rows, d] view whose map is 3-D over
+// (col, row, b*H + h) when `rank3`, else 4-D over (col, row, h, b).
+__device__ __forceinline__ void tma_load_view(uint32_t dst, const void* tmap, bool rank3, int col, int row, int h,
+                                              int b, int bh, uint32_t bar) {
+    if (rank3) tma_load_3d(dst, tmap, col, row, bh, bar);
+    else tma_load_4d(dst, tmap, col, row, h, b, bar);
+}
+
 // 3-D tiled reduce-add of one box from shared memory into global memory
 // (element-wise atomic add in L2; rows outside the tensor are skipped).
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {

@@ -22,7 +22,9 @@
  *   Layout   q, k, v, o, dO, dq, dk, dv are contiguous [B, H, S, d] arrays of
  *            the element type `dtype` (row-major, d fastest).  lse is a
  *            contiguous [B, H, S] fp32 array holding the natural-log L.
- *            Self-attention only: queries and keys share the length S.
+ *            Queries and keys share the length S, except in fa_fwd_strided /
+ *            fa_bwd_strided, which take N_q query rows and N_k key rows and
+ *            strided views (see there).
  *   Causal   causal != 0 keeps key j for query i only when j <= i
  *            (top-left aligned, square).
  *   Pointers every array argument is a DEVICE pointer of the current CUDA
@@ -77,6 +79,29 @@ typedef enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * Forward pass on general shapes (handout Algorithm 1 as stated: Q in
+ * R^{N_q x d}, K, V in R^{N_k x d}), with strided operands.
+ *   q, o       [B, H, Sq, d] views; k, v [B, H, Sk, d] views.  Each view is
+ *              given by a HOST array of three element strides {batch, head,
+ *              row}; the head dimension is contiguous (stride 1).  NULL
+ *              means contiguous.  A stride whose dimension has more than one
+ *              index must be positive and a multiple of 16 bytes (8 bf16 or 4
+ *              fp32 elements); FA_ERR_MISALIGNED otherwise.  o must not
+ *              overlap itself or the inputs.
+ *   lse        contiguous [B, H, Sq] fp32.
+ *   Sq, Sk     N_q >= 0 and N_k >= 1 (N_k = 0 with N_q > 0 is
+ *              FA_ERR_INVALID_ARG: the softmax over no key is undefined).
+ *   causal     keeps key j for query i when j <= i (indices from 0 in both,
+ *              top-left aligned): with Sk > Sq the last keys are never seen,
+ *              with Sq > Sk the last queries see every key.
+ * Everything else as fa_fwd; fa_fwd(...) equals fa_fwd_strided with NULL
+ * strides and Sq = Sk = S.
+ */
+int fa_fwd_strided(const void* q, const long long* q_strides, const void* k, const long long* k_strides,
+                   const void* v, const long long* v_strides, void* o, const long long* o_strides, float* lse,
+                   int B, int H, int Sq, int Sk, int d, int causal, float scale, int dtype, void* stream);
 
 /*
  * Split-KV building block ("[Attention] FlashAttention/Ring-Attention/...统一
@@ -151,6 +176,27 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
                          const float* lse, void* dq, void* dk, void* dv,
                          void* workspace, size_t workspace_bytes,
                          int B, int H, int S, int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * Backward pass on general shapes and strided operands; the counterpart of
+ * fa_fwd_strided (same view, size and causal conventions).
+ *   q, o, dO, dq   [B, H, Sq, d] views; k, v, dk, dv [B, H, Sk, d] views, each
+ *                  with its own host stride array (NULL: contiguous).
+ *   lse            contiguous [B, H, Sq] fp32 from the forward.
+ *   workspace      >= fa_bwd_workspace_size(B, H, Sq, d, dtype) bytes
+ *                  (B*H*Sq*4 with deterministic != 0), 256-byte aligned.
+ *   deterministic  0: dQ by fp32 atomics as fa_bwd; otherwise dQ by its own
+ *                  pass as fa_bwd_deterministic.
+ * With Sq = 0 and Sk > 0 only dk and dv are written (zeros).  Keys that no
+ * query attends under the causal mask get dk = dv = 0.
+ */
+int fa_bwd_strided(const void* q, const long long* q_strides, const void* k, const long long* k_strides,
+                   const void* v, const long long* v_strides, const void* o, const long long* o_strides,
+                   const void* dO, const long long* do_strides, const float* lse,
+                   void* dq, const long long* dq_strides, void* dk, const long long* dk_strides,
+                   void* dv, const long long* dv_strides, void* workspace, size_t workspace_bytes,
+                   int B, int H, int Sq, int Sk, int d, int causal, float scale, int dtype, int deterministic,
+                   void* stream);
 
 /*
  * Backward pass for callers that cannot allocate device memory.

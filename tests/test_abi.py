@@ -124,3 +124,26 @@ def test_deterministic_bwd_workspace_rules_need_no_gpu(lib):
     assert det(P, B * H * S * 4, d=48) == -2
     assert fa.fa_bwd_deterministic(None, None, None, None, None, None, None, None, None, None, 0,
                                    0, 2, 128, 64, 1, 0.125, 0, None) == 0
+
+
+def test_strided_and_rectangular_argument_errors_need_no_gpu(lib):
+    """fa_fwd_strided / fa_bwd_strided check strides and N_k before any launch."""
+    P = ctypes.c_void_p(A)
+    st = lambda *x: (ctypes.c_longlong * 3)(*x)
+    good = st(2 * 64 * 128, 64 * 128, 64)
+    fwd = lambda qs=good, ks=good, Sq=128, Sk=128, B=2, H=2, dtype=0: lib.fa_fwd_strided(
+        P, qs, P, ks, P, good, P, good, P, B, H, Sq, Sk, 64, 1, 0.125, dtype, None)
+    assert fwd(ks=st(0, 64 * 128, 64)) == -1 and b"not positive" in lib.fa_get_last_error()
+    assert fwd(qs=st(2 * 64 * 128, 64 * 128, 68)) == -3 and b"16 bytes" in lib.fa_get_last_error()
+    assert fwd(Sk=0) == -1 and b"no key rows" in lib.fa_get_last_error()
+    assert fwd(Sq=0) == 0                                  # nothing to compute
+    # A stride of a dimension with one index is never used, so it is not checked.
+    assert fwd(qs=st(0, 0, 64), B=1, H=1, Sk=0) == -1     # fails on Sk, not on the strides
+    ws = ctypes.c_void_p(A)
+    bwd = lambda Sq, Sk, ws_bytes=1 << 30, dk=P: lib.fa_bwd_strided(
+        P, None, P, None, P, None, P, None, P, None, P, P, None, dk, None, P, None, ws, ws_bytes,
+        1, 2, Sq, Sk, 64, 1, 0.125, 0, 0, None)
+    assert bwd(128, 0) == -1
+    assert bwd(128, 256, ws_bytes=16) == -4
+    assert bwd(0, 256, dk=ctypes.c_void_p(0)) == -1       # no queries: dk, dv still written, so checked
+    assert bwd(0, 0) == 0

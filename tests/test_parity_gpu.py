@@ -450,3 +450,103 @@ def test_deterministic_autograd_matches_atomic():
         grads.append([t.grad.cpu() for t in (qd, kd, vd)])
     assert torch.equal(grads[0][1], grads[1][1]) and torch.equal(grads[0][2], grads[1][2])
     assert_close("dq", grads[1][0], f64(grads[0][0]), *TOL["bf16"]["grad"])
+
+
+# ---------------------------------------------------------------- general shapes: N_q != N_k, strided views
+from seeded_inputs import make_inputs_rect  # noqa: E402
+
+
+def _run_rect(q, k, v, do, causal, scale, deterministic=False):
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal, scale)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, dod, lse, causal, scale, deterministic=deterministic)
+    fa.check_status()
+    return [t.cpu() for t in (o, lse, dq, dk, dv)]
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("bf16", 80), ("fp32", 32)])
+@pytest.mark.parametrize("Sq,Sk", [(200, 333), (333, 200), (128, 640), (640, 128), (1, 300), (300, 1)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_rectangular_lengths_match_oracle(dtype, d, Sq, Sk, causal):
+    """N_q != N_k (Algorithms 1 and 2 as stated), causal top-left, both
+    backward forms, every head against the oracle."""
+    q, k, v, do = make_inputs_rect(1, 2, Sq, Sk, d, dtype, seed=8300 + Sq + 7 * Sk + d)
+    scale = 1 / math.sqrt(d)
+    tol = TOL[dtype]
+    res = _run_rect(q, k, v, do, causal, scale)
+    det = _run_rect(q, k, v, do, causal, scale, deterministic=True)
+    for h in range(2):
+        r = oracle_head(q, k, v, do, 0, h, causal, scale, dtype)
+        tag = f"[h={h},Sq={Sq},Sk={Sk},causal={causal}]"
+        assert_close("O" + tag, res[0][0, h], r["O"], *tol["o"])
+        assert_close("L" + tag, res[1][0, h], r["L"], *tol["lse"])
+        for name, i in (("dq", 2), ("dk", 3), ("dv", 4)):
+            assert_close(name + tag, res[i][0, h], r[name], *tol["grad"])
+            assert_close(name + " deterministic" + tag, det[i][0, h], r[name], *tol["grad"])
+    if causal and Sk > Sq:
+        # Keys past the last query are never attended: exactly zero gradients.
+        assert torch.count_nonzero(res[3][:, :, Sq:]) == 0 and torch.count_nonzero(res[4][:, :, Sq:]) == 0
+
+
+def _layout(t, kind):
+    """The same values as contiguous t [B, H, S, d] in another memory layout."""
+    B, H, S, d = t.shape
+    if kind == "bshd":            # [B, S, H, d] storage, viewed as [B, H, S, d]
+        return t.transpose(1, 2).contiguous().transpose(1, 2)
+    if kind == "padded":          # rows of d + 16 elements, the first d used
+        buf = torch.zeros((B, H, S, d + 16), dtype=t.dtype, device=t.device)
+        buf[..., :d] = t
+        return buf[..., :d]
+    if kind == "hbsd":            # [H, B, S, d] storage
+        return t.transpose(0, 1).contiguous().transpose(0, 1)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 96), ("fp32", 64)])
+@pytest.mark.parametrize("kind", ["bshd", "padded", "hbsd"])
+def test_strided_views_give_bitwise_the_contiguous_results(dtype, d, kind):
+    """Strides change only the addressing: O, L, dK, dV and the deterministic
+    dQ must equal the contiguous call's bit for bit; the outputs are written
+    into views of the same layout."""
+    B, H, Sq, Sk = 2, 3, 257, 190
+    q, k, v, do = (t.to(DEV) for t in make_inputs_rect(B, H, Sq, Sk, d, dtype, seed=8400 + d))
+    scale = 1 / math.sqrt(d)
+    ref_o, ref_l = fa.fwd(q, k, v, True, scale)
+    ref_g = fa.bwd(q, k, v, ref_o, do, ref_l, True, scale, deterministic=True)
+    ref_ga = fa.bwd(q, k, v, ref_o, do, ref_l, True, scale)
+    qs, ks, vs, dos = (_layout(t, kind) for t in (q, k, v, do))
+    assert not qs.is_contiguous()
+    o_s = _layout(torch.zeros_like(q), kind)
+    o, l = fa.fwd(qs, ks, vs, True, scale, out=o_s)
+    grads_out = tuple(_layout(torch.zeros_like(t), kind) for t in (q, k, v))
+    g = fa.bwd(qs, ks, vs, o, dos, l, True, scale, out=grads_out, deterministic=True)
+    ga = fa.bwd(qs, ks, vs, o, dos, l, True, scale, out=tuple(_layout(torch.zeros_like(t), kind) for t in (q, k, v)))
+    fa.check_status()
+    assert o.data_ptr() == o_s.data_ptr()
+    assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+    for name, a, b in zip(("dq", "dk", "dv"), g, ref_g):
+        assert torch.equal(a, b), f"{name} ({kind}) differs from the contiguous call"
+    assert torch.equal(ga[1], ref_ga[1]) and torch.equal(ga[2], ref_ga[2])
+    assert_close("dq atomic strided", ga[0].cpu(), f64(ref_ga[0].cpu()), *TOL[dtype]["grad"])
+    if kind == "padded":
+        # The padding columns of the output views were not touched.
+        assert torch.count_nonzero(o_s.as_strided((B, H, Sq, 16), o_s.stride(), d)) == 0
+
+
+def test_backward_with_no_queries_zeroes_dk_dv():
+    k, v = (torch.randn(1, 2, 200, 64, device=DEV).to(torch.bfloat16) for _ in range(2))
+    q = torch.empty(1, 2, 0, 64, device=DEV, dtype=torch.bfloat16)
+    o, lse = fa.fwd(q, k, v, False)
+    dq, dk, dv = fa.bwd(q, k, v, o, torch.empty_like(q), lse, False,
+                        out=(torch.empty_like(q), torch.full_like(k, 7.0), torch.full_like(v, 7.0)))
+    fa.check_status()
+    assert o.shape == (1, 2, 0, 64) and torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+def test_misaligned_stride_is_refused():
+    """A row stride of 68 bf16 elements (136 bytes) cannot be a TMA stride: the
+    call is refused on the host with FA_ERR_MISALIGNED, nothing is launched."""
+    base = torch.randn(1, 2, 64, 68 + 4, device=DEV).to(torch.bfloat16)
+    qv = base.as_strided((1, 2, 16, 64), (2 * 64 * 72, 64 * 72, 68, 1))   # row stride 68: 136 bytes
+    with pytest.raises(fa.FAError):
+        fa.fwd(qv, qv, qv, False)
