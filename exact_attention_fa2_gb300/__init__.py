@@ -133,9 +133,18 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
 
 
-def _stream_handle(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(stream, device_index=None) -> int:
+    """cudaStream_t of `stream` (a torch stream or an int); None = the current
+    stream of `device_index` (default: the current device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if device_index is None:
+            device_index = torch.cuda.current_device()
+        if _raw_stream is not None:
+            return int(_raw_stream(device_index))
+        stream = torch.cuda.current_stream(device_index)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -146,20 +155,24 @@ def _ptr(t):
 def _check_qkv(*ts):
     """q, k, v (then o, dO): [B, H, N, d] CUDA tensors of one dtype and device
     with a contiguous head dimension; q (o, dO) share N_q, k and v share N_k.
-    Other strides are passed to the library, which checks their alignment."""
+    Other strides are passed to the library, which checks their alignment.
+    Returns the device index."""
     q = ts[0]
-    if q.dim() != 4:
-        raise ValueError("expected [B, H, S, d] tensors")
+    dev = q.get_device()
+    if dev < 0:
+        raise ValueError("tensors must be on a CUDA device (there is no CPU fallback)")
+    qs, ks = q.shape, ts[1].shape
+    if len(qs) != 4 or len(ks) != 4 or ks[0] != qs[0] or ks[1] != qs[1] or ks[3] != qs[3]:
+        raise ValueError("q, o, dO must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
+    dt = q.dtype
     for i, t in enumerate(ts):
-        if not t.is_cuda:
-            raise ValueError("tensors must be on a CUDA device (there is no CPU fallback)")
-        if t.dtype != q.dtype or t.device != q.device or t.dim() != 4:
-            raise ValueError("q, k, v (and o, dO) must share dtype, device and rank 4")
+        if t.dtype is not dt or t.get_device() != dev:
+            raise ValueError("q, k, v (and o, dO) must share dtype and CUDA device")
+        if t.shape != (ks if i in (1, 2) else qs):
+            raise ValueError("q, o, dO must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
         if t.stride(-1) != 1:
             raise ValueError("the head dimension (last) must be contiguous")
-        ref = q if i in (0, 3, 4) else ts[1]
-        if t.shape != ref.shape or t.shape[0] != q.shape[0] or t.shape[1] != q.shape[1] or t.shape[3] != q.shape[3]:
-            raise ValueError("q, o, dO must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
+    return dev
 
 
 def _plain(*ts):
@@ -201,25 +214,34 @@ def check_status(stream=None):
 
 def fwd(q, k, v, causal: bool = False, scale=None, out=None, lse=None, stream=None):
     """Forward pass; returns (o, lse)."""
-    _check_qkv(q, k, v)
+    dev = _check_qkv(q, k, v)
+    if dev != torch.cuda.current_device():
+        with torch.cuda.device(dev):
+            return fwd(q, k, v, causal, scale, out, lse, stream)
     B, H, S, d = q.shape
     Sk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    o = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32) if lse is None else lse
-    _check_qkv(q, k, v, o)
-    if not lse.is_contiguous() or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S):
+    if out is None:
+        o = torch.empty_like(q)
+    else:
+        o = out
+        _check_qkv(q, k, v, o)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    elif not lse.is_contiguous() or lse.dtype is not torch.float32 or tuple(lse.shape) != (B, H, S):
         raise ValueError("lse must be a contiguous fp32 [B, H, N_q] tensor")
-    st = ctypes.c_void_p(_stream_handle(stream))
-    with torch.cuda.device(q.device):
-        if _plain(q, k, v, o):
-            rc = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, S, d, causal, scale,
-                        _dtype_code(q), st)
-        else:
-            rc = load_library().fa_fwd_strided(
-                _ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o), _strides(o), _ptr(lse),
-                B, H, S, Sk, d, int(causal), scale, _dtype_code(q), st)
-    _check(rc)
+    lib = _lib or load_library()
+    st = _stream_handle(stream, dev)
+    code = _dtype_code(q)
+    if _plain(q, k, v, o):
+        rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, S, d,
+                        int(causal), scale, code, st)
+    else:
+        rc = lib.fa_fwd_strided(
+            q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v), o.data_ptr(),
+            _strides(o), lse.data_ptr(), B, H, S, Sk, d, int(causal), scale, code, st)
+    if rc:
+        _check(rc)
     return o, lse
 
 
@@ -229,34 +251,40 @@ def bwd(q, k, v, o, do, lse, causal: bool = False, scale=None, workspace=None, s
     reported by bwd_workspace_size) is allocated here when not given.
     ``deterministic`` selects fa_bwd_deterministic: dQ from its own
     query-tile-outer pass, bitwise reproducible."""
-    _check_qkv(q, k, v, o, do)
+    dev = _check_qkv(q, k, v, o, do)
+    if dev != torch.cuda.current_device():
+        with torch.cuda.device(dev):
+            return bwd(q, k, v, o, do, lse, causal, scale, workspace, stream, out, deterministic)
     B, H, S, d = q.shape
     Sk = k.shape[2]
+    if lse.dtype is not torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * S or lse.get_device() != dev:
+        raise ValueError("lse must be the forward's contiguous fp32 [B, H, N_q] tensor")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = _dtype_code(q)
-    need = bwd_workspace_size(B, H, S, d, code)
+    lib = _lib or load_library()
     if workspace is None:
+        need = int(lib.fa_bwd_workspace_size(B, H, S, d, code))
         workspace = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
-    _check_qkv(q, k, v, o, do)
-    _check_qkv(dq, dk, dv, q, q)
-    st = ctypes.c_void_p(_stream_handle(stream))
+        _check_qkv(dq, dk, dv, q, q)
+    st = _stream_handle(stream, dev)
     nbytes = workspace.numel() * workspace.element_size()
-    with torch.cuda.device(q.device):
-        if _plain(q, k, v, o, do, dq, dk, dv):
-            entry = fa_bwd_deterministic if deterministic else fa_bwd
-            rc = entry(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                       _ptr(dv), _ptr(workspace), nbytes, B, H, S, d, causal, scale, code, st)
-        else:
-            rc = load_library().fa_bwd_strided(
-                _ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o), _strides(o),
-                _ptr(do), _strides(do), _ptr(lse), _ptr(dq), _strides(dq), _ptr(dk), _strides(dk),
-                _ptr(dv), _strides(dv), _ptr(workspace), nbytes, B, H, S, Sk, d, int(causal), scale, code,
-                int(bool(deterministic)), st)
-    _check(rc)
+    if _plain(q, k, v, o, do, dq, dk, dv):
+        entry = lib.fa_bwd_deterministic if deterministic else lib.fa_bwd
+        rc = entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), nbytes, B, H, S, d,
+                   int(causal), scale, code, st)
+    else:
+        rc = lib.fa_bwd_strided(
+            q.data_ptr(), _strides(q), k.data_ptr(), _strides(k), v.data_ptr(), _strides(v), o.data_ptr(),
+            _strides(o), do.data_ptr(), _strides(do), lse.data_ptr(), dq.data_ptr(), _strides(dq), dk.data_ptr(),
+            _strides(dk), dv.data_ptr(), _strides(dv), workspace.data_ptr(), nbytes, B, H, S, Sk, d, int(causal),
+            scale, code, int(bool(deterministic)), st)
+    if rc:
+        _check(rc)
     return dq, dk, dv
 
 

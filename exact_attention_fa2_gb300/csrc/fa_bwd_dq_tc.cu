@@ -392,7 +392,7 @@ cudaError_t bwd_dq_tc_launch(const BwdArgs& a) {
     p.scale = a.scale;
     p.neg_a = a.scale < 0.f ? 1u : 0u;
     auto kern = bwd_dq_tc_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
+    cudaError_t e = set_smem_limit<bwd_dq_tc_kernel<D>>(G::DYN_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_q * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }

@@ -637,7 +637,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     p.scale = a.scale;
     p.neg_a = a.scale < 0.f ? 1u : 0u;
     auto kern = bwd_tc_kernel<D, WITH_DQ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
+    cudaError_t e = set_smem_limit<bwd_tc_kernel<D, WITH_DQ>>(G::DYN_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_kv * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }

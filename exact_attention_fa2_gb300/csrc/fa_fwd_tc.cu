@@ -568,7 +568,7 @@ cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o
     p.c = c < 1e-30f ? 1e-30f : c;
     p.neg_a = a.scale < 0.f ? 1u : 0u;
     auto kern = fwd_tc_kernel<D, PARTIAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::DYN_SMEM);
+    cudaError_t e = set_smem_limit<fwd_tc_kernel<D, PARTIAL>>(G::DYN_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_units * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
 }

@@ -5,6 +5,7 @@
 #include <stddef.h>
 
 #include <algorithm>
+#include <atomic>
 
 namespace fa {
 
@@ -57,6 +58,23 @@ struct BwdArgs {
     int Sk;                 // N_k
     View vq, vk, vv, vo, vdo, vdq, vdk, vdv;   // q, o, dO, dq: [B,H,S,d]; k, v, dk, dv: [B,H,Sk,d]
 };
+
+// Raise `kern`'s dynamic shared-memory limit to `bytes`, once per device
+// (the attribute persists in the context; setting it on every launch costs a
+// driver call).  A cudaDeviceReset inside the process is not tracked: the
+// next launch of the kernel then fails with a launch error.
+template <auto KERN>
+cudaError_t set_smem_limit(int bytes) {
+    static std::atomic<unsigned long long> done{0};   // bit i: set on device i (< 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Launch `kern` as a programmatic dependent of the previous kernel on the
 // stream: its blocks may start while that kernel drains and must execute

@@ -470,7 +470,7 @@ template <typename T, int D>
 cudaError_t fwd_simt_launch(const FwdArgs& a, int kb, int ke, T* o, View vo) {
     constexpr size_t smem = fwd_smem_bytes<D>();
     auto kern = fwd_simt_kernel<T, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit<fwd_simt_kernel<T, D>>((int)smem);
     if (e != cudaSuccess) return e;
     const int n_qtiles = (a.S + BQ - 1) / BQ;
     dim3 grid(n_qtiles, a.B * a.H);
@@ -483,7 +483,7 @@ template <typename T, int D>
 cudaError_t bwd_simt_launch(const BwdArgs& a) {
     constexpr size_t smem = bwd_smem_bytes<D>();
     auto kern = bwd_simt_kernel<T, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit<bwd_simt_kernel<T, D>>((int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Sk + BK - 1) / BK, a.B * a.H);
     kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, a.vq, (const T*)a.k, a.vk, (const T*)a.v, a.vv,
@@ -496,7 +496,7 @@ template <typename T, int D>
 cudaError_t bwd_dq_simt_launch(const BwdArgs& a) {
     constexpr size_t smem = sizeof(float) * (size_t)(64 * (D + 1) * 4 + 64 * LDP + 2 * 64);
     auto kern = bwd_dq_simt_kernel<T, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit<bwd_dq_simt_kernel<T, D>>((int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.S + BQ - 1) / BQ, a.B * a.H);
     kern<<<grid, NT, smem, a.stream>>>((const T*)a.q, a.vq, (const T*)a.k, a.vk, (const T*)a.v, a.vv,
