@@ -92,6 +92,8 @@ def load_library():
         lib.fa_fwd_bwd_host_buffer_size.restype = sz
         lib.fa_fwd_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_bwd_host.restype = i
+        lib.fa_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
+        lib.fa_selftest_bounded_wait.restype = i
         lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_strided.restype = i
         lib.fa_bwd_strided.argtypes = ([vp] * 17 + [vp, sz] + [i, i, i, i, i, i, f, i, i, vp])

@@ -6,6 +6,7 @@
 #include "fa_gb300.h"
 #include "fa_common.cuh"
 #include "fa_launch.h"
+#include "sm103_ptx.cuh"
 
 #include <cmath>
 #include <cstdarg>
@@ -514,6 +515,42 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dO,
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev[2], 0);
     if (e != cudaSuccess) return done(cuda_fail(e, "gradient copies"));
     return done(FA_OK);
+}
+
+}  // extern "C"
+
+namespace {
+
+// One thread waits, through the bounded wait every kernel uses, for an
+// mbarrier phase that nothing completes; it gives up after limit_ns, sets
+// the status word and returns.
+__global__ void selftest_wait_kernel(unsigned int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        fa::sm103::mbar_init(fa::sm103::smem_u32(&bar), 1);
+        abort_flag = 0;
+        fa::sm103::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) fa::sm103::mbar_wait(fa::sm103::smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_selftest_bounded_wait(unsigned long long limit_ns, void* stream) {
+    g_err[0] = 0;
+    if (limit_ns == 0 || limit_ns > 10000000000ull)
+        return fail(FA_ERR_INVALID_ARG, "limit %llu ns is outside (0, 10 s]", limit_ns);
+    unsigned int* status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc) return rc;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return FA_OK;
 }
 
 int fa_check_status(void* stream) {

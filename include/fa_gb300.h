@@ -270,6 +270,18 @@ const char* fa_get_last_error(void);
  */
 int fa_check_status(void* stream);
 
+/*
+ * Self-test of device-side failure detection.  Every wait inside the
+ * library's kernels is bounded: after its limit (2 s) the kernel sets the
+ * device status word, the CTA's other roles give up too, and the kernel
+ * returns, leaving the CUDA context usable; fa_check_status then reports
+ * FA_ERR_DEVICE_TIMEOUT.  This call enqueues one tiny kernel on `stream` whose
+ * single wait can never complete (a barrier phase nothing arrives at) and
+ * gives up after limit_ns nanoseconds (0 < limit_ns <= 10 s), exercising that
+ * path.  Returns FA_OK once enqueued; FA_ERR_INVALID_ARG for a bad limit.
+ */
+int fa_selftest_bounded_wait(unsigned long long limit_ns, void* stream);
+
 /* Library version as 10000*major + 100*minor + patch. */
 int fa_version(void);
 

@@ -147,3 +147,8 @@ def test_strided_and_rectangular_argument_errors_need_no_gpu(lib):
     assert bwd(128, 256, ws_bytes=16) == -4
     assert bwd(0, 256, dk=ctypes.c_void_p(0)) == -1       # no queries: dk, dv still written, so checked
     assert bwd(0, 0) == 0
+
+
+def test_selftest_limit_checked_without_launch(lib):
+    assert lib.fa_selftest_bounded_wait(ctypes.c_ulonglong(0), None) == -1
+    assert lib.fa_selftest_bounded_wait(ctypes.c_ulonglong(20_000_000_000), None) == -1

@@ -550,3 +550,21 @@ def test_misaligned_stride_is_refused():
     qv = base.as_strided((1, 2, 16, 64), (2 * 64 * 72, 64 * 72, 68, 1))   # row stride 68: 136 bytes
     with pytest.raises(fa.FAError):
         fa.fwd(qv, qv, qv, False)
+
+
+def test_bounded_wait_runs_out_and_is_reported_then_the_context_works():
+    """Failure detection on the device: a wait that can never complete gives
+    up after its limit, the kernel returns, the host reads
+    FA_ERR_DEVICE_TIMEOUT, and the next calls run normally."""
+    import ctypes
+    lib = fa.load_library()
+    assert lib.fa_selftest_bounded_wait(ctypes.c_ulonglong(20_000_000), None) == 0
+    with pytest.raises(fa.FAError) as e:
+        fa.check_status()
+    assert e.value.code == -6 and "bounded wait" in str(e.value)
+    fa.check_status()                                      # the word was cleared
+    q, k, v, do = make_inputs(1, 2, 256, 64, "bf16", seed=8500)
+    o, lse, dq, dk, dv, _ = run_gpu(q, k, v, do, True, 0.125)
+    r = oracle_head(q, k, v, do, 0, 1, True, 0.125, "bf16")
+    assert_close("O after the timeout", o[0, 1], r["O"], *TOL["bf16"]["o"])
+    assert_close("dQ after the timeout", dq[0, 1], r["dq"], *TOL["bf16"]["grad"])
