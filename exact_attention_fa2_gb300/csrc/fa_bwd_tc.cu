@@ -64,6 +64,9 @@ constexpr int SMEM_BUDGET = 227 * 1024;
 template <int D>
 struct BwdTm {
     static constexpr bool PIPE = D <= 64;
+    // d <= 32: dQ_i is issued by a second thread (in the dQ read-out warps);
+    // its products are the cheapest, so one issuing thread limits the most.
+    static constexpr bool SPLIT_DQ = D <= 32;
     static constexpr uint32_t DV = 0;
     static constexpr uint32_t DK = PIPE ? 64 : 128;
     static constexpr uint32_t DQ = PIPE ? 128 : TM_DP;
@@ -91,8 +94,8 @@ struct BwdCfg {
     static constexpr int LD_OFF = QD_OFF + NS * 2 * TILE;
     static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
     // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain,
-    // s_free, p_free, ds_free[2]
-    static constexpr int NBARS = 12 + 2 * NS;
+    // s_free, p_free, ds_free[2], drain_dq
+    static constexpr int NBARS = 13 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t s_free = s_full + 56;      // S^T and dP^T have been read (pipelined schedule)
     const uint32_t p_free = s_full + 64;      // dV has read P^T
     auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dS^T buffer b (holding the staged dQ) is free
+    const uint32_t drain_dq = s_full + 88;    // the dQ issuer's products have finished (abort only)
     using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
@@ -219,6 +223,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(p_free, 1);
         mbar_init(ds_free(0), 1);
         mbar_init(ds_free(1), 1);
+        mbar_init(drain_dq, 1);
         *abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -352,7 +357,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
                     if constexpr (!WITH_DQ) mma_commit(ds_free(it & 1));   // dK has read dS^T
                 }
-                if constexpr (!WITH_DQ) {
+                if constexpr (!WITH_DQ || TM::SPLIT_DQ) {
+                    // (d <= 32: dQ_i = dS K is issued by a thread of the dQ read-out warps.)
                     __syncwarp();
                     continue;
                 }
@@ -523,10 +529,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const int qr = wq * 32 + lane;                 // query row inside the tile
         const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + TM::DQ;
         const bool leader = threadIdx.x == DQ_WARP0 * 32;
+        // d <= 32: lane 0 of the next warp issues dQ_i = dS K, beside the main
+        // issuer (one thread issues a product only every ~80-100 cycles).
+        const bool dq_issuer = TM::SPLIT_DQ && warp == DQ_WARP0 + 1;
+        bool iss_ok = true;
+        if (dq_issuer) iss_ok = warp_wait(kv_full, 0, abort, p.status);   // K is resident
         griddep_wait();                                // the dQ accumulator is zeroed by the previous kernel
         for (int it = 0; it < n_it; ++it) {
             const int s = it % NS;
+            if (dq_issuer) {
+                // dS^T of tile it is in shared memory and dQ_{i-1} has been read out.
+                if (!(iss_ok = iss_ok && warp_wait(p_full, it & 1, abort, p.status))) break;
+                if (it > 0 && !(iss_ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t dso = (uint32_t)((it & 1) * G::DS_BYTES) >> 4;
+                    const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, 128 * 128);
+                    const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
+                        const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, desc_hi(1024, SW_128B));
+                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(dq_full);
+                }
+                __syncwarp();
+            }
             if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
+            // d <= 32: dK (the other issuer's) must also have read dS^T before
+            // the tile is staged over it; its commit completes q_empty.
+            if (TM::SPLIT_DQ && !warp_wait(q_empty(s), (it / NS) & 1, abort, p.status)) break;
             tc_fence_after();
             // Stage this row box by box in the TMA swizzle: for d <= 64 into
             // the dS^T buffer that dK and dQ_i have just read (dQ_i is 32 KB
@@ -579,6 +611,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             if ((warp == DQ_WARP0) && __shfl_sync(0xffffffffu, lead_ok, 0) == 0) break;
         }
         if (leader) bulk_wait_all();
+        if (dq_issuer && *abort) {
+            // Every product this thread issued has finished before TMEM is freed.
+            if (lane == 0) {
+                volatile int no_abort = 0;
+                mma_commit(drain_dq);
+                mbar_wait(drain_dq, 0, &no_abort, p.status, WAIT_LIMIT_NS);
+            }
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
