@@ -464,7 +464,8 @@ def _run_rect(q, k, v, do, causal, scale, deterministic=False):
     return [t.cpu() for t in (o, lse, dq, dk, dv)]
 
 
-@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("bf16", 80), ("fp32", 32)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("bf16", 80), ("bf16", 32), ("bf16", 16),
+                                     ("fp32", 32)])
 @pytest.mark.parametrize("Sq,Sk", [(200, 333), (333, 200), (128, 640), (640, 128), (1, 300), (300, 1)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_rectangular_lengths_match_oracle(dtype, d, Sq, Sk, causal):
