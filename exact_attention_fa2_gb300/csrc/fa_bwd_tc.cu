@@ -131,6 +131,7 @@ struct BwdParams {
     View vdk, vdv;        // element strides of dk, dv
     uint32_t map3;        // bit i: map i of (q, k, v, dO) is 3-D over (col, row, b*H + h)
     int H;
+    int grp;              // heads per group of the grid order
     int S;                // query rows N_q
     int Sk;               // key rows N_k
     int n_q;
@@ -194,10 +195,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // One flat grid ordered key-tile-major: early key tiles see the most query
-    // tiles under the causal mask, so every head's heaviest tile goes first.
+    // tiles under the causal mask, so every head's heaviest tile goes first
+    // (within head groups when the heads' tiles would not stay in L2 together).
     const int BH = (int)(gridDim.x / (unsigned)p.n_kv);
-    const int j = (int)blockIdx.x / BH;
-    const int bh = (int)blockIdx.x - j * BH;
+    int j, bh;
+    if (p.grp >= BH) {
+        j = (int)blockIdx.x / BH;
+        bh = (int)blockIdx.x - j * BH;
+    } else {
+        grid_unit((int)blockIdx.x, BH, p.n_kv, p.grp, j, bh);
+    }
     const int bb = bh / p.H, hh = bh - bb * p.H;
     const int S = p.S;
     const int k0 = j * BK;
@@ -672,6 +679,8 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     // Causal: key tiles past the last query tile are attended by no query;
     // their zero gradients are written by a separate launch.
     if (a.causal) p.n_kv = std::min(p.n_kv, p.n_q);
+    // Each CTA streams its head's Q, dO (bf16) and, with dQ, the fp32 dQ rows.
+    p.grp = head_group(BH, p.n_kv, (4.0 + (WITH_DQ ? 4.0 : 0.0)) * a.S * D);
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;

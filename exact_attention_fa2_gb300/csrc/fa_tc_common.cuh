@@ -39,6 +39,38 @@ struct Chunks {
     static constexpr bool SINGLE_N = D == 128 || PAD;
 };
 
+// Block b of a flat grid of n_units units for each of BH heads, ordered in
+// groups of grp heads: inside a group every head's unit 0 comes first, then
+// every head's unit 1, and so on (grp = BH: one group, plain unit-major order).
+__device__ __forceinline__ void grid_unit(int b, int BH, int n_units, int grp, int& unit, int& bh) {
+    const int per = grp * n_units;
+    const int g = b / per;
+    const int g0 = g * grp;
+    const int gsz = min(grp, BH - g0);
+    const int r = b - g * per;
+    unit = r / gsz;
+    bh = g0 + r - unit * gsz;
+}
+
+// Heads per group of that order for a kernel whose CTAs each stream
+// `bytes_per_head` of their head's data from L2.  All heads (the plain
+// longest-first order) while every head's data fits 160 MB; beyond that, as
+// few heads as give the GPU two waves of units, within 64 MB, so the CTAs in
+// flight re-read a few heads' tiles from L2 instead of DRAM.  Smaller groups
+// than needed would cost more in load balance (the heaviest units of later
+// groups start late) than they save.
+inline int head_group(int BH, int n_units, double bytes_per_head) {
+    constexpr double kMB = 1024.0 * 1024.0;
+    if (BH * bytes_per_head <= 160.0 * kMB) return BH;
+    int sms = 152, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int g = (2 * sms + n_units - 1) / n_units;
+    const int cap = (int)(64.0 * kMB / bytes_per_head);
+    g = g < cap ? g : cap;
+    g = g < 1 ? 1 : g;
+    return g < BH ? g : BH;
+}
+
 // Lane 0 waits, the rest of the warp learns the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           unsigned int* status) {
