@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
         const float l2 = row < S ? p.lse[grow] * FA_LOG2E : INFINITY;   // P = 0 on rows past S
         const float dd = row < S ? p.Dvec[grow] : 0.f;
         const float c = p.c;
+        const uint64_t c2 = f2pack(c, c);
+        const uint64_t nl2 = f2pack(-l2, -l2);
+        const uint64_t ndd = f2pack(-dd, -dd);
         const int key_lim = p.causal ? min(row, p.Sk - 1) : p.Sk - 1;
         bool ok = true;
         for (int j = 0; j < nj; ++j) {
@@ -308,15 +311,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
             // Only the diagonal tile and a ragged last tile need the per-key mask.
             const bool masked = (p.causal && j == qt) || ((j + 1) * BK > p.Sk);
             uint32_t pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                float p0 = ex2(fmaf(__uint_as_float(rs[2 * e]), c, -l2));
-                float p1 = ex2(fmaf(__uint_as_float(rs[2 * e + 1]), c, -l2));
-                if (masked) {
+            // P = exp2(S c - L2), dS = P (dP - D) in f32x2 pairs.
+            auto pair = [&](int e, bool mask) {
+                float p0, p1;
+                f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2, nl2), p0, p1);
+                p0 = ex2(p0);
+                p1 = ex2(p1);
+                if (mask) {
                     if (kbase + 2 * e > key_lim) p0 = 0.f;
                     if (kbase + 2 * e + 1 > key_lim) p1 = 0.f;
                 }
-                pk[e] = pack_bf16(p0 * (__uint_as_float(rp[2 * e]) - dd), p1 * (__uint_as_float(rp[2 * e + 1]) - dd));
+                float d0, d1;
+                f2unpack(mul2(f2pack(p0, p1),
+                              add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])), ndd)), d0, d1);
+                pk[e] = pack_bf16(d0, d1);
+            };
+            if (masked) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pair(e, true);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pair(e, false);
             }
             const int b = j & 1;
             // dQ += dS_{j-2} K_{j-2} has read this buffer.

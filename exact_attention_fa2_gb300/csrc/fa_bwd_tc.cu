@@ -269,17 +269,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             const int s = it % NS;
             const uint32_t ph = (it / NS) & 1;
             const int q0 = (i0 + it) * BQ;
-            // (L * log2 e, D) for the 128 query rows, loaded before the stage
-            // is free so that the loads overlap the wait; rows past S get
-            // (+inf, 0) so that P = 0.  D (and the zeroed dQ accumulator)
-            // come from the previous kernel.
+            // (-L * log2 e, -D) for the 128 query rows, loaded before the
+            // stage is free so that the loads overlap the wait; rows past S
+            // get (-inf, 0) so that P = 0.  D (and the zeroed dQ
+            // accumulator) come from the previous kernel.
             if (it == 0) griddep_wait();
             float l2[BQ / 32], dd[BQ / 32];
 #pragma unroll
             for (int e = 0; e < BQ / 32; ++e) {
                 const int q = q0 + e * 32 + lane;
-                l2[e] = q < S ? p.lse[rb + q] * FA_LOG2E : INFINITY;
-                dd[e] = q < S ? p.Dvec[rb + q] : 0.f;
+                l2[e] = q < S ? -p.lse[rb + q] * FA_LOG2E : -INFINITY;
+                dd[e] = q < S ? -p.Dvec[rb + q] : 0.f;
             }
             if (!warp_wait(q_empty(s), ph ^ 1, abort, p.status)) break;
             if (lane == 0) {
@@ -292,10 +292,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                                   bb, bh, q_full(s));
                 }
             }
+            // Stored per pair of rows (2r, 2r+1) as (-L2_2r, -L2_2r+1, -D_2r,
+            // -D_2r+1), the operand pairs of the packed f32x2 arithmetic.
 #pragma unroll
-            for (int e = 0; e < BQ / 32; ++e)
-                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" :: "r"(sb + G::LD_OFF + s * G::LD_BYTES + (e * 32 + lane) * 8),
-                             "f"(l2[e]), "f"(dd[e]) : "memory");
+            for (int e = 0; e < BQ / 32; ++e) {
+                const int r = e * 32 + lane;
+                const uint32_t a = sb + G::LD_OFF + s * G::LD_BYTES + (r >> 1) * 16 + (r & 1) * 4;
+                asm volatile("st.shared.f32 [%0], %1;" :: "r"(a), "f"(l2[e]) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" :: "r"(a + 8), "f"(dd[e]) : "memory");
+            }
             mbar_arrive(q_full(s));
             issued = it + 1;
         }
@@ -441,6 +446,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t tS = tmem + lane_off + TM_S;
         const uint32_t tP = tmem + lane_off + TM_DP;
         const float c = p.c;
+        const uint64_t c2 = f2pack(c, c);
         const uint32_t ds_row = sb + G::DS_OFF + jr * 128;
         const uint32_t swz = (uint32_t)(jr & 7);
         bool ok = true;
@@ -466,18 +472,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
                 }
                 uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                // P = exp2(S c - L2) and dS = P (dP - D) in f32x2 pairs; only
+                // the diagonal tile and a ragged key tile need the mask.
+                auto pair = [&](int e, bool mask) {
                     const int q = 32 * qq + 2 * e;                          // query column inside the tile
-                    const float4 ld = ld_shared_f4(ldb + q * 8);           // (L2, D) of q and q+1
-                    float p0 = ex2(fmaf(__uint_as_float(rs[2 * e]), c, -ld.x));
-                    float p1 = ex2(fmaf(__uint_as_float(rs[2 * e + 1]), c, -ld.z));
-                    if (!key_ok || (diag && q < jr)) p0 = 0.f;
-                    if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
-                    const float d0 = p0 * (__uint_as_float(rp[2 * e]) - ld.y);
-                    const float d1 = p1 * (__uint_as_float(rp[2 * e + 1]) - ld.w);
+                    const float4 ld = ld_shared_f4(ldb + q * 8);           // (-L2, -D) of q and q+1
+                    float p0, p1;
+                    f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2,
+                                  f2pack(ld.x, ld.y)), p0, p1);
+                    p0 = ex2(p0);
+                    p1 = ex2(p1);
+                    if (mask) {
+                        if (!key_ok || (diag && q < jr)) p0 = 0.f;
+                        if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
+                    }
+                    const uint64_t p2 = f2pack(p0, p1);
+                    float d0, d1;
+                    f2unpack(mul2(p2, add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
+                                           f2pack(ld.z, ld.w))), d0, d1);
                     pk[e] = pack_bf16(p0, p1);
                     dk[e] = pack_bf16(d0, d1);
+                };
+                if (diag || !key_ok) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pair(e, true);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pair(e, false);
                 }
                 if (TM::PIPE && qh == 0) {
                     // P^T and dS^T buffers of earlier tiles must have been read.
