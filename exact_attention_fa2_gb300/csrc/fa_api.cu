@@ -194,7 +194,7 @@ HostStepLayout host_step_layout(int B, int H, int S, int d, int dtype) {
     HostStepLayout L;
     L.arr = align_up(rows * d * elt, 256);
     L.lse = align_up(rows * sizeof(float), 256);
-    L.ws = align_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
+    L.ws = fa_bwd_workspace_size(B, H, S, d, dtype);
     L.total = 8 * L.arr + L.lse + L.ws;
     return L;
 }
