@@ -95,7 +95,7 @@ struct BwdCfg {
     static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
     // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain,
     // s_free, p_free, ds_free[2], drain_dq
-    static constexpr int NBARS = 13 + 2 * NS;
+    static constexpr int NBARS = 14 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     const uint32_t p_free = s_full + 64;      // dV has read P^T
     auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dS^T buffer b (holding the staged dQ) is free
     const uint32_t drain_dq = s_full + 88;    // the dQ issuer's products have finished (abort only)
+    const uint32_t dp_full = s_full + 96;     // d > 64: dP^T is in Tensor Memory (s_full: S^T alone)
     using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(ds_free(0), 1);
         mbar_init(ds_free(1), 1);
         mbar_init(drain_dq, 1);
+        mbar_init(dp_full, 1);
         *abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -393,12 +395,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
             if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
             tc_fence_after();
-            if (lane == 0) mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);         // S^T = K Q^T
+            if (lane == 0) {
+                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                    // S^T = K Q^T
+                mma_commit(s_full);                    // P^T can be formed while dP^T waits for its columns
+            }
             if (WITH_DQ && it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
             tc_fence_after();
             if (lane == 0) {
                 mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
-                mma_commit(s_full);
+                mma_commit(dp_full);
             }
             if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
             tc_fence_after();
@@ -458,64 +463,129 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             if (!(ok = warp_wait(s_full, it & 1, abort, p.status))) break;
             tc_fence_after();
             const uint32_t ldb = sb + G::LD_OFF + s * G::LD_BYTES;
-#pragma unroll
-            for (int qh = 0; qh < 2; ++qh) {
-                const int qq = 2 * h + qh;                                  // 32-query quarter of the tile
-                uint32_t rs[32], rp[32];
-                tmem_ld32(tS + 32 * qq, rs);
-                tmem_ld32(tP + 32 * qq, rp);
-                tmem_wait_ld();
-                reg_fence<32>(rs);
-                reg_fence<32>(rp);
-                if (TM::PIPE && qh == 1) {
-                    tc_fence_before();
-                    mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
-                }
-                uint32_t pk[16], dk[16];
-                // P = exp2(S c - L2) and dS = P (dP - D) in f32x2 pairs; only
-                // the diagonal tile and a ragged key tile need the mask.
-                auto pair = [&](int e, bool mask) {
-                    const int q = 32 * qq + 2 * e;                          // query column inside the tile
-                    const float4 ld = ld_shared_f4(ldb + q * 8);           // (-L2, -D) of q and q+1
-                    float p0, p1;
-                    f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2,
-                                  f2pack(ld.x, ld.y)), p0, p1);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    if (mask) {
-                        if (!key_ok || (diag && q < jr)) p0 = 0.f;
-                        if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
-                    }
-                    const uint64_t p2 = f2pack(p0, p1);
-                    float d0, d1;
-                    f2unpack(mul2(p2, add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
-                                           f2pack(ld.z, ld.w))), d0, d1);
-                    pk[e] = pack_bf16(p0, p1);
-                    dk[e] = pack_bf16(d0, d1);
-                };
-                if (diag || !key_ok) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pair(e, true);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pair(e, false);
-                }
-                if (TM::PIPE && qh == 0) {
-                    // P^T and dS^T buffers of earlier tiles must have been read.
-                    if (it > 0 && !(ok = warp_wait(p_free, (it - 1) & 1, abort, p.status))) break;
-                    if (it > 1 && !(ok = warp_wait(ds_free(it & 1), ((it >> 1) - 1) & 1, abort, p.status))) break;
-                    tc_fence_after();
-                }
-                // P^T of these 32 queries: 16 columns of bf16 pairs (for
-                // d > 64 inside this half's own, already read, score columns).
-                tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
-                // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
-                // 128-byte-swizzled [key][query] tile (two 64-query chunks).
+            // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
+            // 128-byte-swizzled [key][query] tile (two 64-query chunks).
+            auto store_ds = [&](int qh, const uint32_t* dk) {
                 const uint32_t chunk = ds_row + (uint32_t)((it & 1) * (G::NDS - 1) * G::DS_BYTES) + (uint32_t)h * 16384;
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
                     const uint32_t u = (uint32_t)(qh * 4 + u4);
                     st_shared_v4(chunk + ((u ^ swz) << 4), dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
+                }
+            };
+            if constexpr (TM::PIPE) {
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh) {
+                    const int qq = 2 * h + qh;                                  // 32-query quarter of the tile
+                    uint32_t rs[32], rp[32];
+                    tmem_ld32(tS + 32 * qq, rs);
+                    tmem_ld32(tP + 32 * qq, rp);
+                    tmem_wait_ld();
+                    reg_fence<32>(rs);
+                    reg_fence<32>(rp);
+                    if (qh == 1) {
+                        tc_fence_before();
+                        mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
+                    }
+                    uint32_t pk[16], dk[16];
+                    // P = exp2(S c - L2) and dS = P (dP - D) in f32x2 pairs; only
+                    // the diagonal tile and a ragged key tile need the mask.
+                    auto pair = [&](int e, bool mask) {
+                        const int q = 32 * qq + 2 * e;                          // query column inside the tile
+                        const float4 ld = ld_shared_f4(ldb + q * 8);           // (-L2, -D) of q and q+1
+                        float p0, p1;
+                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2,
+                                      f2pack(ld.x, ld.y)), p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        if (mask) {
+                            if (!key_ok || (diag && q < jr)) p0 = 0.f;
+                            if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
+                        }
+                        const uint64_t p2 = f2pack(p0, p1);
+                        float d0, d1;
+                        f2unpack(mul2(p2, add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
+                                               f2pack(ld.z, ld.w))), d0, d1);
+                        pk[e] = pack_bf16(p0, p1);
+                        dk[e] = pack_bf16(d0, d1);
+                    };
+                    if (diag || !key_ok) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pair(e, true);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pair(e, false);
+                    }
+                    if (qh == 0) {
+                        // P^T and dS^T buffers of earlier tiles must have been read.
+                        if (it > 0 && !(ok = warp_wait(p_free, (it - 1) & 1, abort, p.status))) break;
+                        if (it > 1 && !(ok = warp_wait(ds_free(it & 1), ((it >> 1) - 1) & 1, abort, p.status))) break;
+                        tc_fence_after();
+                    }
+                    // P^T of these 32 queries: 16 columns of bf16 pairs.
+                    tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
+                    store_ds(qh, dk);
+                }
+            } else {
+                // d > 64, in two phases: P^T from S^T (the exponentials) as soon
+                // as S^T is in, while dP^T waits for the previous dQ_i's
+                // columns; then dS^T once dP^T is in.  P stays in registers
+                // between the phases.
+                float pf[2][32];
+                auto p_of = [&](int qq, const uint32_t* rs, float* pv, bool mask) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int q = 32 * qq + 2 * e;
+                        const float4 ld = ld_shared_f4(ldb + q * 8);       // (-L2, -D) of q and q+1
+                        float p0, p1;
+                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2,
+                                      f2pack(ld.x, ld.y)), p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        if (mask) {
+                            if (!key_ok || (diag && q < jr)) p0 = 0.f;
+                            if (!key_ok || (diag && q + 1 < jr)) p1 = 0.f;
+                        }
+                        pv[2 * e] = p0;
+                        pv[2 * e + 1] = p1;
+                    }
+                };
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh) {
+                    const int qq = 2 * h + qh;
+                    uint32_t rs[32];
+                    tmem_ld32(tS + 32 * qq, rs);
+                    tmem_wait_ld();
+                    reg_fence<32>(rs);
+                    if (diag || !key_ok) p_of(qq, rs, pf[qh], true);
+                    else p_of(qq, rs, pf[qh], false);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(pf[qh][2 * e], pf[qh][2 * e + 1]);
+                    // P^T of these 32 queries inside this half's own, already
+                    // read, score columns.
+                    tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
+                }
+                if (!(ok = warp_wait(dp_full, it & 1, abort, p.status))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int qh = 0; qh < 2; ++qh) {
+                    const int qq = 2 * h + qh;
+                    uint32_t rp[32];
+                    tmem_ld32(tP + 32 * qq, rp);
+                    tmem_wait_ld();
+                    reg_fence<32>(rp);
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float4 ld = ld_shared_f4(ldb + (32 * qq + 2 * e) * 8);
+                        float d0, d1;
+                        f2unpack(mul2(f2pack(pf[qh][2 * e], pf[qh][2 * e + 1]),
+                                      add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
+                                           f2pack(ld.z, ld.w))), d0, d1);
+                        dk[e] = pack_bf16(d0, d1);
+                    }
+                    store_ds(qh, dk);
                 }
             }
             if (!ok) break;
