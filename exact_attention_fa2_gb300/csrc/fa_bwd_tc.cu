@@ -94,8 +94,8 @@ struct BwdCfg {
     static constexpr int LD_OFF = QD_OFF + NS * 2 * TILE;
     static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
     // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain,
-    // s_free, p_free, ds_free[2], drain_dq
-    static constexpr int NBARS = 14 + 2 * NS;
+    // s_free, p_free, ds_free[2], drain_dq, dp_full, dst_full
+    static constexpr int NBARS = 15 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
     auto ds_free = [&](int b) { return s_full + 72u + 8u * b; };   // dS^T buffer b (holding the staged dQ) is free
     const uint32_t drain_dq = s_full + 88;    // the dQ issuer's products have finished (abort only)
     const uint32_t dp_full = s_full + 96;     // d > 64: dP^T is in Tensor Memory (s_full: S^T alone)
+    const uint32_t dst_full = s_full + 104;   // d > 64: dS^T is in shared memory (p_full: P^T alone)
     using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(ds_free(1), 1);
         mbar_init(drain_dq, 1);
         mbar_init(dp_full, 1);
+        mbar_init(dst_full, 2 * BK);
         *abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -389,47 +391,71 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 __syncwarp();
             }
         }
-        for (int it = 0; it < n_it && ok && !TM::PIPE; ++it) {
-            const int s = it % NS;
-            const uint32_t ph = (it / NS) & 1;
-            const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
-            if (!(ok = warp_wait(q_full(s), ph, abort, p.status))) break;
-            tc_fence_after();
-            if (lane == 0) {
-                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                    // S^T = K Q^T
-                mma_commit(s_full);                    // P^T can be formed while dP^T waits for its columns
+        if constexpr (!TM::PIPE) {
+            // d > 64: dV of tile it goes in as soon as P^T is in Tensor
+            // Memory, so it runs while dS^T is formed; dK and dQ_i follow
+            // dS^T, and S^T of tile it+1 follows them into the columns that
+            // held P^T (one thread's products run in issue order).  dP^T of
+            // tile it+1 waits for the read-out of dQ_i, which shares its
+            // columns; its commit also covers dK and dQ_i, which have then
+            // read the one dS^T buffer.
+            auto issue_s = [&](int it) {
+                const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
+                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
+                mma_commit(s_full);
+            };
+            if (ok) ok = warp_wait(q_full(0), 0, abort, p.status);
+            if (ok) {
+                tc_fence_after();
+                if (lane == 0) issue_s(0);
+                __syncwarp();
             }
-            if (WITH_DQ && it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
-            tc_fence_after();
-            if (lane == 0) {
-                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
-                mma_commit(dp_full);
-            }
-            if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
-            tc_fence_after();
-            if (lane == 0) {
-                // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
-                                        ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
-                    const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int s = it % NS;
+                const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
+                if (WITH_DQ && it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);             // dP^T = V dO^T
+                    mma_commit(dp_full);
                 }
-                if constexpr (WITH_DQ) {
+                if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
-                        const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
-                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < BQ / 16; ++ks)
+                        mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
+                                            ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                if (!(ok = warp_wait(dst_full, it & 1, abort, p.status))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
+                        const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
+                        mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                     }
-                    mma_commit(dq_full);
-                } else {
-                    mma_commit(q_empty(s));             // Q_i, dO_i (and L, D) are no longer read
+                    if constexpr (WITH_DQ) {
+#pragma unroll
+                        for (int ks = 0; ks < BK / 16; ++ks) {                              // dQ_i = dS K
+                            const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
+                            mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(dq_full);
+                    } else {
+                        mma_commit(q_empty(s));         // Q_i, dO_i (and L, D) are no longer read
+                    }
+                }
+                __syncwarp();
+                if (it + 1 < n_it) {
+                    if (!(ok = warp_wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1, abort, p.status))) break;
+                    tc_fence_after();
+                    if (lane == 0) issue_s(it + 1);
+                    __syncwarp();
                 }
             }
-            __syncwarp();
         }
         if (ok && lane == 0) mma_commit(done);
         if (*abort) {
@@ -566,6 +592,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     // read, score columns.
                     tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full);                                    // dV may read P^T
                 if (!(ok = warp_wait(dp_full, it & 1, abort, p.status))) break;
                 tc_fence_after();
 #pragma unroll
@@ -589,10 +618,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
             if (!ok) break;
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(p_full);
+            if constexpr (TM::PIPE) {
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            } else {
+                fence_proxy_async_smem();
+                tc_fence_before();                     // dP^T has been read: dQ_i may take its columns
+                mbar_arrive(dst_full);
+            }
         }
         // dK, dV rows of this key tile (16-column units split between the halves).
         if (ok && warp_wait(done, 0, abort, p.status)) {
