@@ -1,0 +1,105 @@
+"""Host-side logic of bench.py, checked without a GPU: the FLOP count, the
+workload names, the peak table, the summary of the clock samples (throttle
+reasons) and the rule that a stored DRAM-traffic figure is reported only
+while the kernel source it was measured on is unchanged."""
+import hashlib
+import importlib.util
+import json
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_flop_count_is_two_products_per_head(bench):
+    """Forward FLOPs: S = Q K^T and O = P V, each S*S*d multiply-adds per
+    (batch, head); causal counts half the score matrix.  Counted here by
+    walking a tiny problem's multiply-adds."""
+    w = bench.Workload("tiny", 2, 3, 5, 4, "bf16", (True,), 1.0, 0)
+    madds = 0
+    for _ in range(w.B * w.H):
+        for _i in range(w.S):
+            for _j in range(w.S):
+                madds += w.d          # one score
+                madds += w.d          # its row of P times V
+    assert bench.flops_fwd(w, causal=False) == 2 * madds
+    assert bench.flops_fwd(w, causal=True) == madds
+
+
+def test_workload_names(bench):
+    w = bench.workload("sweep:8192:128")
+    assert (w.B, w.H, w.S, w.d, w.dtype) == (1, 16, 8192, 128, "bf16")
+    assert bench.workload("sweep:1024:32:fp32").dtype == "fp32"
+    c2 = bench.workload("c2")
+    assert (c2.B, c2.H, c2.S, c2.d) == (4, 12, 1024, 64)
+    with pytest.raises(SystemExit):
+        bench.workload("no-such-workload")
+
+
+def test_peaks_fall_back_without_the_measured_table(bench, tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    pk = bench.load_peaks()
+    assert pk["source"] == "fallback" and pk["hbm_gbs"] == 6800.0 and pk["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.0, "bf16_tflops": 1950.0}))
+    pk = bench.load_peaks()
+    assert pk["source"] == "measured" and pk["bf16_tflops_sustained"] == 1950.0
+
+
+def _row(sm, mx, hw="Not Active", thermal="Not Active", sw_thermal="Not Active", power="Not Active"):
+    return ["2026/01/01 00:00:00.000", "0", str(sm), str(mx), "850.0", "0x0", hw, thermal, sw_thermal, power]
+
+
+def test_clock_summary_median_and_reasons(bench):
+    cs = bench.ClockSampler(0)
+    cs.rows = [(10.0, _row(1900, 2070)), (10.1, _row(2000, 2070, power="Active")),
+               (10.2, _row(2070, 2070)), (50.0, _row(300, 2070, hw="Active"))]   # last one outside the window
+    s = cs.summary(10.0, 10.2)
+    assert s["sm_mhz"] == 2000.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+    s = cs.summary(49.9, 50.1)
+    assert s["reasons"] == ["hw_slowdown"] and s["sm_mhz"] == 300.0
+
+
+def test_clock_summary_without_samples(bench):
+    cs = bench.ClockSampler(0)
+    s = cs.summary(0.0, 1.0)
+    assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == ["no samples"]
+    cs.rows = [(5.0, _row("[N/A]", "[N/A]"))]        # unreadable fields are skipped, not parsed
+    s = cs.summary(100.0, 101.0)                     # no row in the window: all rows are used
+    assert s["samples"] == 1 and s["sm_mhz"] is None and s["sm_max_mhz"] is None
+
+
+def test_traffic_used_only_while_the_source_is_unchanged(bench, tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("k", "c2") is None                          # no record at all
+    src = tmp_path / "kern.cu"
+    src.write_bytes(b"__global__ void k() {}\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    rec = {"k": {"c2": {"source": "kern.cu", "source_sha256_16": sha, "dram_bytes_per_launch": 1234}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.load_traffic("k", "c2") == 1234
+    assert bench.load_traffic("k", "c3") is None                          # other workload
+    assert bench.load_traffic("other", "c2") is None                      # other kernel
+    src.write_bytes(b"__global__ void k() { /* changed */ }\n")
+    assert bench.load_traffic("k", "c2") is None                          # stale figure dropped
+
+
+def test_committed_traffic_record_is_well_formed():
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    assert rec, "empty traffic record"
+    for kern, by_workload in rec.items():
+        for wl, ent in by_workload.items():
+            assert os.path.exists(os.path.join(ROOT, ent["source"])), (kern, wl)
+            assert os.path.exists(os.path.join(ROOT, ent["from"])), (kern, wl)
+            assert len(ent["source_sha256_16"]) == 16
+            assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
