@@ -25,7 +25,9 @@
 // once; Q_i, dO_i per tile, plus L and D), warp 13 Tensor Memory allocation
 // and the single-thread MMA issuer.
 // Tensor Memory columns: dV [0,128), dK [128,256), S^T/P^T [256,384),
-// dP^T [384,512), which dQ_i reuses once dS^T has been formed.
+// dP^T [384,512), which dQ_i reuses once dS^T has been formed.  With this
+// layout (d > 64) the products of tile i are issued as S^T; dP^T once dQ_{i-1}
+// has been read out; dV once P^T is in; dK and dQ_i once dS^T is in.
 // Shapes: N_q queries and N_k keys (Algorithm 2's Q in R^{N_q x d}, K, V in
 // R^{N_k x d}), causal keeping key j for query i when j <= i; every
 // [B, H, rows, d] operand is a view with strides that are multiples of 8
@@ -489,14 +491,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             if (!(ok = warp_wait(s_full, it & 1, abort, p.status))) break;
             tc_fence_after();
             const uint32_t ldb = sb + G::LD_OFF + s * G::LD_BYTES;
-            // dS^T row, queries 32qq..32qq+31: four 16-byte units of the
-            // 128-byte-swizzled [key][query] tile (two 64-query chunks).
-            auto store_ds = [&](int qh, const uint32_t* dk) {
+            // dS^T row, queries 32qq..32qq+31 (dsp: 16 bf16 pairs): four
+            // 16-byte units of the 128-byte-swizzled [key][query] tile (two
+            // 64-query chunks).
+            auto store_ds = [&](int qh, const uint32_t* dsp) {
                 const uint32_t chunk = ds_row + (uint32_t)((it & 1) * (G::NDS - 1) * G::DS_BYTES) + (uint32_t)h * 16384;
 #pragma unroll
                 for (int u4 = 0; u4 < 4; ++u4) {
                     const uint32_t u = (uint32_t)(qh * 4 + u4);
-                    st_shared_v4(chunk + ((u ^ swz) << 4), dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
+                    st_shared_v4(chunk + ((u ^ swz) << 4), dsp[4 * u4], dsp[4 * u4 + 1], dsp[4 * u4 + 2], dsp[4 * u4 + 3]);
                 }
             };
             if constexpr (TM::PIPE) {
@@ -513,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         tc_fence_before();
                         mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
                     }
-                    uint32_t pk[16], dk[16];
+                    uint32_t pk[16], dsp[16];
                     // P = exp2(S c - L2) and dS = P (dP - D) in f32x2 pairs; only
                     // the diagonal tile and a ragged key tile need the mask.
                     auto pair = [&](int e, bool mask) {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         f2unpack(mul2(p2, add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
                                                f2pack(ld.z, ld.w))), d0, d1);
                         pk[e] = pack_bf16(p0, p1);
-                        dk[e] = pack_bf16(d0, d1);
+                        dsp[e] = pack_bf16(d0, d1);
                     };
                     if (diag || !key_ok) {
 #pragma unroll
@@ -550,13 +553,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     }
                     // P^T of these 32 queries: 16 columns of bf16 pairs.
                     tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
-                    store_ds(qh, dk);
+                    store_ds(qh, dsp);
                 }
             } else {
                 // d > 64, in two phases: P^T from S^T (the exponentials) as soon
                 // as S^T is in, while dP^T waits for the previous dQ_i's
-                // columns; then dS^T once dP^T is in.  P stays in registers
-                // between the phases.
+                // columns; p_full then lets dV read P^T while dS^T is formed
+                // once dP^T is in.  P stays in fp32 registers between the phases.
                 float pf[2][32];
                 auto p_of = [&](int qq, const uint32_t* rs, float* pv, bool mask) {
 #pragma unroll
@@ -604,7 +607,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     tmem_ld32(tP + 32 * qq, rp);
                     tmem_wait_ld();
                     reg_fence<32>(rp);
-                    uint32_t dk[16];
+                    uint32_t dsp[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const float4 ld = ld_shared_f4(ldb + (32 * qq + 2 * e) * 8);
@@ -612,9 +615,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                         f2unpack(mul2(f2pack(pf[qh][2 * e], pf[qh][2 * e + 1]),
                                       add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
                                            f2pack(ld.z, ld.w))), d0, d1);
-                        dk[e] = pack_bf16(d0, d1);
+                        dsp[e] = pack_bf16(d0, d1);
                     }
-                    store_ds(qh, dk);
+                    store_ds(qh, dsp);
                 }
             }
             if (!ok) break;
