@@ -444,8 +444,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v_cpu, n_sl, el, thr = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n_sl} (b,h) slices of {w.name} (of {w.B * w.H}), fp64 fwd + "
-                                          f"standard bwd, {el:.1f} s"}
+                                "sample": f"{n_sl} whole (b,h) slices of {w.name}, cycling over its "
+                                          f"{w.B * w.H}; fp64 fwd + standard bwd, {el:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
