@@ -140,7 +140,8 @@ int fa_merge(const float* o_a, const float* lse_a, const float* o_b, const float
  *                         recomputation"; Algorithm 2 step 2), written by fa_bwd;
  *   (zero padding to a 256-byte boundary)
  *   dQacc  [B,H,S,d] fp32 the dQ accumulator that the key-tile-outer kernel adds
- *                         into with fp32 atomics, zeroed by fa_bwd itself.
+ *                         into with fp32 atomic adds (bf16: TMA bulk reduce-adds
+ *                         of whole staged tiles), zeroed by fa_bwd itself.
  * Returns 0 for invalid or empty sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int S, int d, int dtype);
