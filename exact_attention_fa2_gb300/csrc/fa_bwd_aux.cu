@@ -2,7 +2,7 @@
 //
 // preprocess: D_i = rowsum(O * dO)_i in fp32 ("Stanford CS336 Assignment 2
 //   (Systems)" handout, section 4, "backward pass with recomputation": D is
-//   precomputed in global memory; Algorithm 2 step 2), and zeroing of the fp32
+//   precomputed in global memory; Algorithm 2, before its loops), and zeroing of the fp32
 //   dQ accumulator that the key-tile-outer kernel adds into (skipped when
 //   there is none: the deterministic backward sums dQ in its own pass).
 // dq_convert: dq = dQacc * scale rounded to the storage dtype (Eq. 18's 1/sqrt(d)

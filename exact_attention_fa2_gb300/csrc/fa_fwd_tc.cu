@@ -26,7 +26,7 @@
 // overwrites the first 64 columns of S_j (already in registers); S_{j+1} then
 // follows the product P_j V_j.
 //
-// Online softmax (Algorithm 1 lines 10-13) in base 2: scores are scaled by
+// Online softmax (Algorithm 1) in base 2: scores are scaled by
 // c = |scale| * log2(e).  The running max is always the exact max so far, which
 // keeps the dominant probability of a sharp row at exactly 1.0 before the bf16
 // rounding of P (letting the max lag by a few binades doubles the bf16 error of
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             tc_fence_before();
             mbar_arrive(p_full(x));
         }
-        // Epilogue (Algorithm 1 lines 15-18): O / l and L = (m + log2 l) ln 2.
+        // Epilogue (the end of Algorithm 1's outer loop): O / l and L = (m + log2 l) ln 2.
         if (ok && jX < 0) {
             // No admissible key in the window (partial attention only).
             if constexpr (PARTIAL) {

@@ -105,7 +105,7 @@ fwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View 
         load_tile<T, D>(Vs, LDV, vbp, vv.s, kb + kt * BK, ke);
         __syncthreads();
 
-        // S tile (Algorithm 1 line 9), rows ty*4+r, columns tx+16c.
+        // S tile (the score block of Algorithm 1), rows ty*4+r, columns tx+16c.
         float s[4][4];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -135,7 +135,7 @@ fwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View 
         }
         __syncthreads();
 
-        // Online softmax (lines 10-12): four threads per row, 16 columns each.
+        // Online softmax (Algorithm 1's running max and sum): four threads per row, 16 columns each.
         {
             const int row = tid / 4, part = tid % 4;
             float* prow = Ps + row * LDP + part * 16;
@@ -166,7 +166,7 @@ fwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View 
         }
         __syncthreads();
 
-        // O = diag(alpha) O + P V (line 13).
+        // O = diag(alpha) O + P V (Algorithm 1's rescaled accumulator).
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const float al = a_s[ty * 4 + r];
@@ -188,7 +188,7 @@ fwd_simt_kernel(const T* __restrict__ q, View vq, const T* __restrict__ k, View 
     }
     __syncthreads();
 
-    // Epilogue (lines 15-18): O / l, L = (m + log2 l) * ln 2.
+    // Epilogue (the end of Algorithm 1's outer loop): O / l, L = (m + log2 l) * ln 2.
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int lr = ty * 4 + r;

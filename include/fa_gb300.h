@@ -137,7 +137,7 @@ int fa_merge(const float* o_a, const float* lse_a, const float* o_b, const float
 /*
  * Bytes of device workspace fa_bwd needs.  The workspace holds, in order,
  *   D      [B,H,S] fp32   D_i = rowsum(O * dO)_i (handout, "backward pass with
- *                         recomputation"; Algorithm 2 step 2), written by fa_bwd;
+ *                         recomputation"; Algorithm 2, before its loops), written by fa_bwd;
  *   (zero padding to a 256-byte boundary)
  *   dQacc  [B,H,S,d] fp32 the dQ accumulator that the key-tile-outer kernel adds
  *                         into with fp32 atomic adds (bf16: TMA bulk reduce-adds

@@ -177,7 +177,7 @@ def round_to_storage(x, dtype: str) -> np.ndarray:
 
 def rowsum_o_do(o, do) -> np.ndarray:
     """D = rowsum(O * dO), handout section 4 "Backward pass with recomputation"
-    (computed once before the backward loops, Algorithm 2 step 2)."""
+    (computed once before the backward loops, Algorithm 2, before its loops)."""
     return np.sum(_f64(o) * _f64(do), axis=-1)
 
 
