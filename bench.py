@@ -71,6 +71,13 @@ def flops_fwd(w: Workload, causal=True) -> float:
     return f / 2 if causal else f
 
 
+def workload_config(w: Workload, causal: bool) -> dict:
+    """The keys of the JSON line's `config` that name the workload; both arms
+    report them alike and add their own timing keys."""
+    return {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
+            "B": w.B, "H": w.H, "S": w.S, "d": w.d, "causal": causal}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -216,8 +223,8 @@ def run_reference(args, world, rank):
         "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
-                   "sample": "one (b,h) slice per step"},
+        "config": {**workload_config(w, True), "sample": "one (b,h) slice per step",
+                   "parallelism": "rank 0 alone, on the host cores"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -411,8 +418,7 @@ def run_ours(args, world, rank, local):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
-                   "B": w.B, "H": w.H, "S": w.S, "d": w.d, "causal": causal,
+        "config": {**workload_config(w, causal),
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "parallelism": f"replica per GPU x{world} (independent heads, no collective)"},
         "frac_of_peak": {"burst": value / peaks["bf16_tflops"],

@@ -103,3 +103,24 @@ def test_committed_traffic_record_is_well_formed():
             assert os.path.exists(os.path.join(ROOT, ent["from"])), (kern, wl)
             assert len(ent["source_sha256_16"]) == 16
             assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
+
+
+def test_reference_arm_line(bench, capsys):
+    """The reference arm (the oracle on the host cores) prints one line with
+    the workload keys both arms share, cpu_baseline = its own value and an
+    e2e object with no host-device traffic."""
+    import types
+    args = types.SimpleNamespace(workload="c1", steps=2, warmup=1, gpus=1)
+    assert bench.run_reference(args, 1, 0) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = bench.workload("c1")
+    for key, val in bench.workload_config(w, True).items():
+        assert line["config"][key] == val
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["unit"] == "TFLOP/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1 and line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert bench.run_reference(args, 2, 1) == 0                      # other ranks: no work, no line
+    assert capsys.readouterr().out == ""
