@@ -234,6 +234,45 @@ def test_two_half_merge_equals_full(causal, split):
     np.testing.assert_allclose(Lm, L[0, 0], atol=1e-14)
 
 
+def test_merge_is_symmetric_associative_and_has_an_identity():
+    """The merge of the partial softmax pieces is the exact combination of
+    two key sets, so its result cannot depend on the order of the sets or on
+    how three sets are grouped, and a set with no admissible key (m = -inf,
+    B = 0) leaves the other unchanged.  A partial over a single key is that
+    key's value row with logsumexp equal to its score."""
+    S, d, sc = 9, 3, 0.8
+    q, k, v = (rnd(120 + s, 1, 1, S, d)[0, 0] for s in range(3))
+    a = oracle.partial_attention(q, k, v, np.array([0, 1, 2]), False, sc)
+    b = oracle.partial_attention(q, k, v, np.array([3, 4]), False, sc)
+    c = oracle.partial_attention(q, k, v, np.array([5, 6, 7, 8]), False, sc)
+    ab = oracle.merge_two_halves(*a, *b)
+    ba = oracle.merge_two_halves(*b, *a)
+    np.testing.assert_allclose(ab[0], ba[0], atol=1e-15)
+    np.testing.assert_allclose(ab[3], ba[3], atol=1e-15)
+    ab_c = oracle.merge_two_halves(*ab[:3], *c)
+    bc = oracle.merge_two_halves(*b, *c)
+    a_bc = oracle.merge_two_halves(*a, *bc[:3])
+    np.testing.assert_allclose(ab_c[0], a_bc[0], atol=1e-14)
+    np.testing.assert_allclose(ab_c[3], a_bc[3], atol=1e-14)
+    O, L = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], False, sc)
+    np.testing.assert_allclose(ab_c[0], O[0, 0], atol=1e-14)
+    # Causal: keys 5..8 are admissible only for queries 5..8; rows 0..4 get
+    # an empty set, which the merge must ignore.
+    e = oracle.partial_attention(q, k, v, np.array([5, 6, 7, 8]), True, sc)
+    assert np.all(np.isneginf(e[1][:5])) and np.all(e[2][:5] == 0) and np.all(e[0][:5] == 0)
+    f = oracle.partial_attention(q, k, v, np.arange(5), True, sc)
+    ef = oracle.merge_two_halves(*f, *e)
+    Oc, Lc = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], True, sc)
+    np.testing.assert_allclose(ef[0], Oc[0, 0], atol=1e-14)
+    np.testing.assert_allclose(ef[3], Lc[0, 0], atol=1e-14)
+    np.testing.assert_array_equal(ef[0][:5], f[0][:5])
+    # One key: the output is that key's value row, the logsumexp its score.
+    o1, m1, b1 = oracle.partial_attention(q, k, v, np.array([4]), False, sc)
+    np.testing.assert_allclose(o1, np.broadcast_to(v[4], o1.shape), atol=1e-15)
+    np.testing.assert_allclose(m1, sc * q @ k[4], atol=1e-15)
+    np.testing.assert_allclose(b1, 1.0, atol=0)
+
+
 def test_sampled_rows_match_full():
     S, d = 12, 4
     q, k, v = (rnd(110 + s, 1, 1, S, d) for s in range(3))
