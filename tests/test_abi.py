@@ -152,3 +152,24 @@ def test_strided_and_rectangular_argument_errors_need_no_gpu(lib):
 def test_selftest_limit_checked_without_launch(lib):
     assert lib.fa_selftest_bounded_wait(ctypes.c_ulonglong(0), None) == -1
     assert lib.fa_selftest_bounded_wait(ctypes.c_ulonglong(20_000_000_000), None) == -1
+
+
+def test_noalloc_limits_need_no_gpu(lib):
+    """fa_bwd_noalloc refuses a problem whose workspace exceeds its built-in
+    scratch before touching the device, naming both sizes; empty problems
+    and unsupported head dims are answered as fa_bwd answers them."""
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    scratch = lib.fa_bwd_noalloc_scratch_bytes()
+    assert scratch == 32 << 20
+    P = ctypes.c_void_p(A)
+    call = lambda B, H, S, d: lib.fa_bwd_noalloc(P, P, P, P, P, P, P, P, P, B, H, S, d, 1, 0.125, fa.FA_BF16, None)
+    need = fa.bwd_workspace_size(1, 16, 8192, 128, fa.FA_BF16)
+    assert need > scratch
+    assert call(1, 16, 8192, 128) == -4
+    msg = lib.fa_get_last_error()
+    assert str(need).encode() in msg and str(scratch).encode() in msg
+    assert call(0, 16, 8192, 128) == 0          # empty: nothing to do
+    assert call(1, 2, 128, 48) == -2            # unsupported head dim
