@@ -2,8 +2,8 @@
 """Benchmark of exact attention (FlashAttention-2 style) on one GB300.
 
 One step = one forward plus one backward pass of causal bf16 attention over
-the B4 H12 S1024 d64 small-LM workload (``c2``), inputs resident in HBM.
-Prints ONE JSON line (rank 0):
+the B4 H32 S4096 d80 2.7B-LM workload (``c4``, Q, K, V ~ 2 N(0,1)), inputs
+resident in HBM.  Prints ONE JSON line (rank 0):
 
   value        fwd+bwd TFLOP/s, FLOPs = 3.5 * 4*B*H*S^2*d * 1/2 (causal), whole job
   e2e          the same metric through fa_fwd_bwd_host, the C-ABI entry on pinned
@@ -11,9 +11,11 @@ Prints ONE JSON line (rank 0):
                inside the timing, steps rotating over three streams
   roofline     the dominant kernel's algorithmic TFLOP/s against the measured peak
   cpu_baseline the fp64 oracle timed on this host's cores on a bounded sample
+  target_shapes  fwd, bwd and fwd+bwd TFLOP/s of B1 H16 S4096/8192 d64/d128
+               causal bf16, with their fractions of the measured bf16 peak
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-        [--workload c2|c3|c4|sweep:S:d]
+        [--workload c2|c3|c4|sweep:S:d] [--no-target-shapes]
 Under torchrun every rank runs its own copy of the workload (independent
 (batch, head) slices: weak scaling, no collective on the data path).
 """
@@ -43,10 +45,12 @@ L2_FLUSH_BYTES = 256 << 20          # > the 129 MB L2
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default="c4")
+    ap.add_argument("--no-target-shapes", action="store_true",
+                    help="skip the B1 H16 S4096/8192 d64/d128 points reported beside the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--memory", action="store_true",
@@ -252,6 +256,92 @@ def load_traffic(kernel_name: str, workload_name: str):
         return None
 
 
+def time_steps(step, n, flush, stream):
+    """Device time (ms) of each of n calls of `step`, CUDA events on the
+    launching stream, L2 flushed before each (outside the events)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def kernel_times(fa, step, n, flush):
+    """{kernel: (total ms, launches)} over n steps from the library's own
+    events around every launch (they serialise the kernels; step times are
+    taken without them)."""
+    fa.profile_read()                      # drop anything recorded so far
+    fa.profile_enable(True)
+    for _ in range(n):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    fa.profile_enable(False)
+    prof = fa.profile_read()
+    fa.check_status()
+    return prof
+
+
+def per_launch_ms(prof, name):
+    tot, n = prof.get(name, (0.0, 0))
+    return tot / n if n else None
+
+
+def bwd_rates(f_fwd, prof):
+    """Backward TFLOP/s on the backward's FLOP count (2.5x the forward's):
+    of the main backward kernel alone, and of the whole backward step
+    (D preprocess + main kernel + dQ conversion, from their own events)."""
+    main = per_launch_ms(prof, "bwd_main")
+    parts = [per_launch_ms(prof, k) for k in ("bwd_preprocess", "bwd_main", "dq_convert")]
+    step_ms = sum(x for x in parts if x) if main else None
+    rate = lambda ms: 2.5 * f_fwd / (ms * 1e-3) / 1e12 if ms else None
+    return {"bwd_kernel_tflops": rate(main), "bwd_step_ms": step_ms, "bwd_step_tflops": rate(step_ms)}
+
+
+TARGET_SHAPES = [(4096, 64), (4096, 128), (8192, 64), (8192, 128)]
+
+
+def measure_target_shapes(fa, dev, flush, stream, peaks, seed_offset):
+    """Causal bf16 B1 H16 at S = 4096, 8192 and d = 64, 128: the shapes the
+    throughput target is stated for.  Each point: whole fwd+bwd steps timed
+    as the main measurement is, then per-kernel times from the library's
+    events."""
+    out = []
+    for S, d in TARGET_SHAPES:
+        w = Workload(f"B1 H16 S{S} d{d}", 1, 16, S, d, "bf16", (True,), 1.0, 4300 + S + d + seed_offset)
+        q, k, v, do = (t.to(dev) for t in make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+        g = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        ws = torch.empty(fa.bwd_workspace_size(w.B, w.H, w.S, w.d, q.dtype), device=dev, dtype=torch.uint8)
+
+        def step():
+            fa.fwd(q, k, v, True, w.scale, out=o, lse=lse)
+            fa.bwd(q, k, v, o, do, lse, True, w.scale, workspace=ws, out=g)
+
+        for _ in range(3):
+            step()
+        fa.check_status()
+        ms = time_steps(step, 20, flush, stream)
+        prof = kernel_times(fa, step, 10, flush)
+        f_fwd = flops_fwd(w, True)
+        ms_step = sum(ms) / len(ms)
+        fwd_ms = per_launch_ms(prof, "fwd")
+        step_tf = 3.5 * f_fwd / (ms_step * 1e-3) / 1e12
+        out.append({"shape": f"B1 H16 S{S} d{d} causal bf16", "fwd_bwd_step_ms": ms_step,
+                    "fwd_bwd_step_tflops": step_tf,
+                    "frac_of_burst_peak": step_tf / peaks["bf16_tflops"],
+                    "frac_of_sustained_peak": step_tf / peaks["bf16_tflops_sustained"],
+                    "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
+                    **bwd_rates(f_fwd, prof)})
+        del q, k, v, do, o, lse, g, ws
+    return out
+
+
 def run_ours(args, world, rank, local):
     import exact_attention_fa2_gb300 as fa
     if not torch.cuda.is_available():
@@ -282,36 +372,20 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()                       # L2 flush between timed steps (outside the events)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = time_steps(step, args.steps, flush, stream)    # L2 flushed between timed steps
     barrier(world)
     t1 = time.time()
     fa.check_status()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world)
 
     # Per-kernel device times from a separate pass with the library's timing
     # events around every launch (they serialise the kernels, so the step
     # time above is taken without them).
     prof_steps = max(5, min(args.steps, 50))
-    fa.profile_read()                      # drop anything recorded so far
-    fa.profile_enable(True)
-    for i in range(prof_steps):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    fa.profile_enable(False)
-    prof = fa.profile_read()
-    fa.check_status()
+    prof = kernel_times(fa, step, prof_steps, flush)
     launches_per_step = sum(v[1] for v in prof.values()) / prof_steps
 
     # The same step with the deterministic backward (fa_bwd_deterministic:
@@ -324,26 +398,11 @@ def run_ours(args, world, rank, local):
     for _ in range(3):
         step_det()
     det_steps = max(5, min(args.steps, 50))
-    ev_det = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(det_steps)]
     barrier(world)
-    torch.cuda.synchronize()
-    for i in range(det_steps):
-        flush.zero_()
-        ev_det[i][0].record(stream)
-        step_det()
-        ev_det[i][1].record(stream)
-    torch.cuda.synchronize()
+    det_ms = time_steps(step_det, det_steps, flush, stream)
     fa.check_status()
-    det_ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_det) / det_steps, world)
-    fa.profile_read()
-    fa.profile_enable(True)
-    for i in range(5):
-        flush.zero_()
-        step_det()
-    torch.cuda.synchronize()
-    fa.profile_enable(False)
-    prof_det = fa.profile_read()
-    fa.check_status()
+    det_ms_per_step = max_over_ranks(sum(det_ms) / det_steps, world)
+    prof_det = kernel_times(fa, step_det, 5, flush)
 
     # End to end through the C ABI with host buffers (fa_fwd_bwd_host): every
     # step copies q, k, v, dO from pinned host memory, runs forward and
@@ -389,6 +448,9 @@ def run_ours(args, world, rank, local):
     e2e_ms_step = max_over_ranks(start.elapsed_time(end) / e2e_steps, world)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
+    targets = None
+    if not args.no_target_shapes:
+        targets = measure_target_shapes(fa, dev, flush, stream, load_peaks(), 7919 * rank)
 
     f_fwd = flops_fwd(w, causal)
     step_flops = 3.5 * f_fwd
@@ -430,7 +492,7 @@ def run_ours(args, world, rank, local):
                     "dq_convert_gbs": (conv_bytes / (per("dq_convert") * 1e-3) / 1e9) if per("dq_convert") else None,
                     "hbm_peak_gbs": peaks["hbm_gbs"],
                     "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
-                    "bwd_tflops": 2.5 * f_fwd / ((ms_per_step - fwd_ms) * 1e-3) / 1e12 if fwd_ms else None,
+                    **bwd_rates(f_fwd, prof),
                     "shares": {k: (v[0] / total_kernel_ms if total_kernel_ms else None) for k, v in prof.items()}},
         "roofline": {"kernel": kernel_names[dom], "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None, "traffic": traffic,
@@ -447,6 +509,12 @@ def run_ours(args, world, rank, local):
                 "api": "fa_fwd_bwd_host (host buffers)", "pipelining": f"steps rotate over {NR} streams"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
     }
+    if targets is not None:
+        line["target_shapes"] = {
+            "what": "causal bf16 B1 H16 at the sequence lengths and head dims the throughput target names; "
+                    "fwd+bwd step timed like `value` (L2 flushed, 20 steps), fwd and bwd from the "
+                    "library's per-kernel events; fractions of the measured bf16 peaks",
+            "points": targets}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v_cpu, n_sl, el, thr = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",

@@ -63,6 +63,11 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int B, int H, int S, int d, int causal, float scale, int dtype, void* stream) {
     const size_t need = fa_bwd_workspace_size(B, H, S, d, dtype);
     if (need > kScratchBytes) {
+        // fa_bwd's own argument checks come first: given no workspace they end
+        // in FA_ERR_WORKSPACE, before any device call, when every other rule
+        // holds; a call that breaks one of them gets that rule's code.
+        const int rc = fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, nullptr, 0, B, H, S, d, causal, scale, dtype, stream);
+        if (rc != FA_ERR_WORKSPACE) return rc;
         char msg[256];
         snprintf(msg, sizeof(msg),
                  "fa_bwd_noalloc: this problem needs %zu bytes of workspace but the built-in scratch holds %zu; "

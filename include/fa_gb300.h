@@ -31,9 +31,15 @@
  *            device, 16-byte aligned.  `stream` is a cudaStream_t passed as
  *            void* (NULL = the legacy default stream).  All work is enqueued
  *            asynchronously on that stream; nothing is synchronised.
- *   Ownership the caller allocates and owns every buffer, including the
- *            backward workspace; the library allocates no device memory and
- *            keeps only host-side state (cached kernel attributes).
+ *   Ownership the caller allocates and owns every buffer it passes,
+ *            including the backward workspace; no call allocates device
+ *            memory.  The library's own device state is static and comes
+ *            with the module when it loads on a device: one status word
+ *            (bounded-wait timeouts, caught indices) and the built-in
+ *            workspace of fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES).  Host
+ *            side it caches kernel attributes and those two arrays' device
+ *            addresses per device, so no cudaDeviceReset may come between
+ *            two calls of this library in one process.
  *   Sizes    B, H, S >= 0 (a zero size is a valid empty problem and returns
  *            FA_OK without launching); d in {16, 32, 64, 80, 96, 128};
  *            B*H <= 65535 and B*H*S*d < 2^31 elements per array.  Any S >= 1 is accepted
@@ -213,6 +219,12 @@ int fa_bwd_strided(const void* q, const long long* q_strides, const void* k, con
  * call allocates nothing.
  *   - Problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
  *     are rejected with FA_ERR_WORKSPACE and a message naming both sizes.
+ *     fa_bwd's argument checks run first, so a call that also breaks one of
+ *     them (a null or misaligned pointer, a size out of range) gets that
+ *     rule's code instead.
+ *   - The array's device address is cached per device after the first call:
+ *     no cudaDeviceReset may come between calls (the cached address would
+ *     then name memory of a context that no longer exists).
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents (D stays readable there; the dQ accumulator is zeroed by every
  *     call).  Calls whose work overlaps on the GPU (different streams, or

@@ -29,6 +29,8 @@ from .attention import (  # noqa: F401
     attention_fwd_rows,
     attention_bwd,
     attention_bwd_from_output,
+    attention_bwd_query_rows,
+    attention_bwd_key_rows,
     round_to_storage,
     rowsum_o_do,
     partial_attention,

@@ -16,8 +16,8 @@ import numpy as np
 
 __all__ = [
     "scores", "causal_keep", "attention_fwd", "attention_fwd_rows", "attention_bwd",
-    "attention_bwd_from_output", "rowsum_o_do", "round_to_storage", "partial_attention",
-    "merge_two_halves",
+    "attention_bwd_from_output", "attention_bwd_query_rows", "attention_bwd_key_rows", "rowsum_o_do",
+    "round_to_storage", "partial_attention", "merge_two_halves",
 ]
 
 
@@ -155,6 +155,60 @@ def attention_bwd_from_output(q, k, v, o, do, L, causal: bool, scale: float):
             dq[b, h] = (dS @ k[b, h]) * scale
             dk[b, h] = (dS.T @ q[b, h]) * scale
     return dq, dk, dv
+
+
+def attention_bwd_query_rows(q_bh, k_bh, v_bh, o_rows, do_rows, L_rows, rows, causal: bool, scale: float):
+    """dQ for chosen query rows of one (b, h) slice: handout Eq. 13-18 read one
+    query row at a time.
+
+    Row i of dQ involves row i of the score matrix and nothing else:
+      S_ij  = scale * Q_i . K_j            (Eq. 13)
+      P_ij  = exp(S_ij - L_i)              (Eq. 14; 0 for keys the mask drops)
+      dP_ij = dO_i . V_j                   (Eq. 16)
+      D_i   = dO_i . O_i                   (rowsum(O * dO))
+      dQ_i  = scale * sum_j P_ij (dP_ij - D_i) K_j     (Eq. 17-18)
+    so sampled rows of a long sequence are exact without the other rows.
+    ``o_rows``, ``do_rows`` and ``L_rows`` are those rows' O (as the forward
+    stored it), dO and L.  Returns dQ rows [r, d].
+    """
+    q_bh, k_bh, v_bh = _f64(q_bh), _f64(k_bh), _f64(v_bh)
+    o_rows, do_rows, L_rows = _f64(o_rows), _f64(do_rows), _f64(L_rows)
+    rows = np.asarray(rows, dtype=np.int64)
+    S_rows = scores(q_bh[rows], k_bh, scale)                       # [r, N_k]
+    P_rows = np.exp(S_rows - L_rows[:, None])
+    if causal:
+        P_rows = np.where(np.arange(k_bh.shape[0])[None, :] <= rows[:, None], P_rows, 0.0)
+    dP_rows = do_rows @ v_bh.T
+    D_rows = np.sum(o_rows * do_rows, axis=1)
+    dS_rows = P_rows * (dP_rows - D_rows[:, None])
+    return (dS_rows @ k_bh) * scale
+
+
+def attention_bwd_key_rows(q_bh, k_bh, v_bh, o_bh, do_bh, L_bh, keys, causal: bool, scale: float):
+    """dK and dV for chosen key rows of one (b, h) slice: handout Eq. 13-17,
+    15 and 19 read one key (one column of the score matrix) at a time.
+
+    Key j's gradients involve column j of P and of dS, hence every query row's
+    L_i and D_i:
+      P_ij  = exp(scale * Q_i . K_j - L_i) (Eq. 13-14; 0 for queries the mask drops)
+      dV_j  = sum_i P_ij dO_i              (Eq. 15)
+      dS_ij = P_ij (dO_i . V_j - D_i)      (Eq. 16-17), D_i = dO_i . O_i
+      dK_j  = scale * sum_i dS_ij Q_i      (Eq. 19)
+    ``o_bh``, ``do_bh``, ``L_bh`` hold every query row.  Returns
+    (dK rows [c, d], dV rows [c, d]).
+    """
+    q_bh, k_bh, v_bh = _f64(q_bh), _f64(k_bh), _f64(v_bh)
+    o_bh, do_bh, L_bh = _f64(o_bh), _f64(do_bh), _f64(L_bh)
+    keys = np.asarray(keys, dtype=np.int64)
+    n_q = q_bh.shape[0]
+    S_cols = scores(q_bh, k_bh[keys], scale)                       # [N_q, c]: columns of S
+    P_cols = np.exp(S_cols - L_bh[:, None])
+    if causal:
+        P_cols = np.where(keys[None, :] <= np.arange(n_q)[:, None], P_cols, 0.0)
+    dP_cols = do_bh @ v_bh[keys].T
+    D = np.sum(o_bh * do_bh, axis=1)
+    dS_cols = P_cols * (dP_cols - D[:, None])
+    return (dS_cols.T @ q_bh) * scale, P_cols.T @ do_bh
 
 
 def round_to_storage(x, dtype: str) -> np.ndarray:

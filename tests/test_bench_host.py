@@ -124,3 +124,30 @@ def test_reference_arm_line(bench, capsys):
                            "d2h_bytes_per_step": 0}
     assert bench.run_reference(args, 2, 1) == 0                      # other ranks: no work, no line
     assert capsys.readouterr().out == ""
+
+
+def test_backward_rates_name_the_kernel_and_the_whole_backward(bench):
+    """The backward's TFLOP/s come from the backward's own event times: one
+    figure for the main backward kernel alone, one for the whole backward
+    (D preprocess + main kernel + dQ conversion); never from a step time."""
+    f_fwd = 1e12
+    prof = {"fwd": (4.0, 4), "bwd_preprocess": (0.4, 4), "bwd_main": (8.0, 4), "dq_convert": (0.8, 4),
+            "dq_pass": (0.0, 0)}
+    r = bench.bwd_rates(f_fwd, prof)
+    assert r["bwd_kernel_tflops"] == pytest.approx(2.5 * f_fwd / 2e-3 / 1e12)
+    assert r["bwd_step_ms"] == pytest.approx(0.1 + 2.0 + 0.2)
+    assert r["bwd_step_tflops"] == pytest.approx(2.5 * f_fwd / 2.3e-3 / 1e12)
+    assert r["bwd_step_tflops"] < r["bwd_kernel_tflops"]
+    # The deterministic backward has no conversion launch: the step is preprocess + main.
+    r = bench.bwd_rates(f_fwd, {"bwd_preprocess": (0.4, 4), "bwd_main": (8.0, 4), "dq_convert": (0.0, 0)})
+    assert r["bwd_step_ms"] == pytest.approx(2.1)
+    assert bench.bwd_rates(f_fwd, {"bwd_main": (0.0, 0)})["bwd_kernel_tflops"] is None
+
+
+def test_default_workload_is_the_largest_single_gpu_config(bench, monkeypatch):
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    args = bench.parse()
+    w = bench.workload(args.workload)
+    assert (w.B, w.H, w.S, w.d, w.qkv_scale) == (4, 32, 4096, 80, 2.0)
+    assert [(S, d) for S, d in bench.TARGET_SHAPES] == [(4096, 64), (4096, 128), (8192, 64), (8192, 128)]

@@ -119,6 +119,23 @@ MUTANTS = [
     ("merge: left weight on the right output", "o = (wl[:, None] * o_l + wr[:, None] * o_r) / Bm[:, None]", 0,
      "o = (wl[:, None] * o_l + wl[:, None] * o_r) / Bm[:, None]"),
     ("merge: logsumexp without the maximum", "return o, m, Bm, m + np.log(Bm)", 0, "return o, m, Bm, np.log(Bm)"),
+    ("query rows: sign of D", "dS_rows = P_rows * (dP_rows - D_rows[:, None])", 0,
+     "dS_rows = P_rows * (dP_rows + D_rows[:, None])"),
+    ("query rows: scale dropped from dQ", "return (dS_rows @ k_bh) * scale", 0, "return dS_rows @ k_bh"),
+    ("query rows: mask drops the diagonal",
+     "P_rows = np.where(np.arange(k_bh.shape[0])[None, :] <= rows[:, None], P_rows, 0.0)", 0,
+     "P_rows = np.where(np.arange(k_bh.shape[0])[None, :] < rows[:, None], P_rows, 0.0)"),
+    ("query rows: D from dO alone", "D_rows = np.sum(o_rows * do_rows, axis=1)", 0,
+     "D_rows = np.sum(do_rows * do_rows, axis=1)"),
+    ("key rows: mask reversed", "P_cols = np.where(keys[None, :] <= np.arange(n_q)[:, None], P_cols, 0.0)", 0,
+     "P_cols = np.where(keys[None, :] >= np.arange(n_q)[:, None], P_cols, 0.0)"),
+    ("key rows: L of the key index", "P_cols = np.exp(S_cols - L_bh[:, None])", 0,
+     "P_cols = np.exp(S_cols - L_bh[keys][None, :])"),
+    ("key rows: dV from dS", "return (dS_cols.T @ q_bh) * scale, P_cols.T @ do_bh", 0,
+     "return (dS_cols.T @ q_bh) * scale, dS_cols.T @ do_bh"),
+    ("key rows: dK from dO in place of Q", "return (dS_cols.T @ q_bh) * scale, P_cols.T @ do_bh", 0,
+     "return (dS_cols.T @ do_bh) * scale, P_cols.T @ do_bh"),
+    ("key rows: dP with K", "dP_cols = do_bh @ v_bh[keys].T", 0, "dP_cols = do_bh @ k_bh[keys].T"),
     ("bf16 rounding: ties not to even", "lsb = (u >> 16) & 1", 0, "lsb = 0 * u"),
     ("bf16 rounding: truncation", "r = ((u + 0x7FFF + lsb) >> 16) << 16", 0, "r = (u >> 16) << 16"),
 ]

@@ -430,3 +430,75 @@ def test_rectangular_causal_keys_past_the_last_query_get_no_gradient():
     dq2, dk2, dv2 = oracle.attention_bwd(q, k[:, :, :nq], v[:, :, :nq], do, True, sc)
     np.testing.assert_allclose(dq, dq2, atol=1e-15)
     np.testing.assert_allclose(dk[:, :, :nq], dk2, atol=1e-15)
+
+
+# ---------------------------------------------------------------- backward on chosen query rows and key rows
+@pytest.mark.parametrize("nq,nk", [(7, 7), (5, 9), (9, 4)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_and_key_backward_match_the_whole_backward(nq, nk, causal):
+    """dQ on chosen query rows and dK, dV on chosen key rows equal the whole
+    matrices of Eq. 13-19, for the exact O and for a perturbed stored O."""
+    d, sc = 4, 0.6
+    q, do = rnd(400 + nq, 1, 1, nq, d), rnd(401, 1, 1, nq, d)
+    k, v = rnd(402 + nk, 1, 1, nk, d), rnd(403, 1, 1, nk, d)
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    rows = [0, nq // 2, nq - 1]
+    keys = [0, nk // 3, nk - 1]
+    for Ost in (O, O + 1e-3 * rnd(404, 1, 1, nq, d)):
+        dq, dk, dv = oracle.attention_bwd_from_output(q, k, v, Ost, do, L, causal, sc)
+        dq_r = oracle.attention_bwd_query_rows(q[0, 0], k[0, 0], v[0, 0], Ost[0, 0, rows], do[0, 0, rows],
+                                               L[0, 0, rows], rows, causal, sc)
+        dk_c, dv_c = oracle.attention_bwd_key_rows(q[0, 0], k[0, 0], v[0, 0], Ost[0, 0], do[0, 0], L[0, 0],
+                                                   keys, causal, sc)
+        np.testing.assert_allclose(dq_r, dq[0, 0, rows], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dk_c, dk[0, 0, keys], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dv_c, dv[0, 0, keys], rtol=1e-12, atol=1e-14)
+
+
+def test_row_and_key_backward_zero_queries_closed_form():
+    """Q = 0, causal, with O and L given by their closed forms (prefix mean of
+    V, log(i+1)): dK_j = 0, dV_j = sum_{i>=j} dO_i/(i+1) and
+    dQ_i = scale * sum_{j<=i} (dO_i.V_j - dO_i.O_i) K_j / (i+1)."""
+    S, d, sc = 11, 4, 0.7
+    q = np.zeros((S, d))
+    k, v, do = rnd(410, S, d), rnd(411, S, d), rnd(412, S, d)
+    n = np.arange(1, S + 1, dtype=np.float64)
+    O = np.cumsum(v, axis=0) / n[:, None]
+    L = np.log(n)
+    rows, keys = [0, 4, 10], [0, 6, 10]
+    dq_r = oracle.attention_bwd_query_rows(q, k, v, O[rows], do[rows], L[rows], rows, True, sc)
+    dk_c, dv_c = oracle.attention_bwd_key_rows(q, k, v, O, do, L, keys, True, sc)
+    for a, i in enumerate(rows):
+        want = sc * sum((do[i] @ v[j] - do[i] @ O[i]) * k[j] for j in range(i + 1)) / (i + 1)
+        np.testing.assert_allclose(dq_r[a], want, rtol=1e-12, atol=1e-14)
+    for a, j in enumerate(keys):
+        np.testing.assert_allclose(dv_c[a], sum(do[i] / (i + 1) for i in range(j, S)), rtol=1e-13, atol=1e-14)
+    assert np.abs(dk_c).max() == 0.0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_and_key_backward_finite_differences(causal):
+    """Central differences of loss = sum(W * O) w.r.t. single rows of Q and
+    single rows of K and V, against the row and key backward fed with the
+    exact O and L (fp64, h = 1e-6)."""
+    S, d, sc, h = 6, 3, 0.55, 1e-6
+    q, k, v, w = (rnd(420 + s, 1, 1, S, d) for s in range(4))
+    O, L = oracle.attention_fwd(q, k, v, causal, sc)
+    rows, keys = [0, 3, 5], [0, 2, 5]
+    dq_r = oracle.attention_bwd_query_rows(q[0, 0], k[0, 0], v[0, 0], O[0, 0, rows], w[0, 0, rows], L[0, 0, rows],
+                                           rows, causal, sc)
+    dk_c, dv_c = oracle.attention_bwd_key_rows(q[0, 0], k[0, 0], v[0, 0], O[0, 0], w[0, 0], L[0, 0], keys, causal, sc)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(w * oracle.attention_fwd(q_, k_, v_, causal, sc)[0]))
+
+    for which, idx, got in ((0, rows, dq_r), (1, keys, dk_c), (2, keys, dv_c)):
+        num = np.zeros((len(idx), d))
+        for a, i in enumerate(idx):
+            for t in range(d):
+                ap = [q.copy(), k.copy(), v.copy()]
+                am = [q.copy(), k.copy(), v.copy()]
+                ap[which][0, 0, i, t] += h
+                am[which][0, 0, i, t] -= h
+                num[a, t] = (loss(*ap) - loss(*am)) / (2 * h)
+        np.testing.assert_allclose(got, num, rtol=1e-6, atol=1e-8)

@@ -35,9 +35,9 @@ def _lib():
     return lib
 
 
-def _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale):
+def _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=None):
     B, H, S, d = q.shape
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     P = lambda t: ctypes.c_void_p(t.data_ptr())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     code = fa.FA_BF16 if q.dtype == torch.bfloat16 else fa.FA_FP32
@@ -57,9 +57,22 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row():
         scale = 1.0 / math.sqrt(d)
         o, lse = fa.fwd(q, k, v, causal, scale)
         ref = fa.bwd(q, k, v, o, do, lse, causal, scale)
-        got = _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale)
+        outs = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
+        # The first call on the device looks up the scratch's address; from
+        # then on a call changes neither PyTorch's allocations nor the
+        # device's free memory.
+        _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[0])
+        torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        got = _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[1])
+        torch.cuda.synchronize()
+        assert (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]) == before
+        # dK and dV come from the same deterministic kernels on both calls.
+        assert torch.equal(outs[0][1], got[1]) and torch.equal(outs[0][2], got[2])
         for name, a, b in zip(("dq", "dk", "dv"), got, ref):
             assert_close(f"{name} {dtype}", a.cpu(), b.cpu(), *TOL[dtype]["grad"])
+        for name, a, b in zip(("dq", "dk", "dv"), outs[0], ref):
+            assert_close(f"{name} {dtype} (first call)", a.cpu(), b.cpu(), *TOL[dtype]["grad"])
 
 
 @pytest.mark.gpu
@@ -73,3 +86,6 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = lib.fa_bwd_noalloc(p, p, p, p, p, p, p, p, p, B, H, S, d, 1, 0.1, fa.FA_BF16, None)
     assert rc == -4
     assert b"built-in scratch" in lib.fa_get_last_error()
+    # An oversized call that also breaks another rule gets that rule's code.
+    rc = lib.fa_bwd_noalloc(p, p, p, p, p, None, p, p, p, B, H, S, d, 1, 0.1, fa.FA_BF16, None)
+    assert rc == -1 and b"lse is null" in lib.fa_get_last_error()
