@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-target-shapes", action="store_true",
                     help="skip the B1 H16 S4096/8192 d64/d128 points reported beside the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lean", action="store_true",
+                    help="only the fwd+bwd steps of --workload (warm-up and timed), one short JSON line: "
+                         "the command the ncu captures run, with nothing else on the device")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--memory", action="store_true",
                     help="instead of timing: peak device memory of fwd+bwd against a materialised-score "
@@ -380,6 +383,15 @@ def run_ours(args, world, rank, local):
     t1 = time.time()
     fa.check_status()
     ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world)
+
+    if args.lean:
+        if rank == 0:
+            f = 3.5 * flops_fwd(w, causal)
+            print(json.dumps({"lean": True, "workload": workload_config(w, causal)["workload"],
+                              "ms_per_step": ms_per_step, "value": world * f / (ms_per_step * 1e-3) / 1e12,
+                              "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup}), flush=True)
+        sampler.stop()
+        return 0
 
     # Per-kernel device times from a separate pass with the library's timing
     # events around every launch (they serialise the kernels, so the step

@@ -213,40 +213,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
         __syncwarp();
     } else if (warp == SDP_WARP) {
         // ------------------------------------------------------------ S / dP issuer
+        // Both issuer roles run on one thread each and wait on the barriers
+        // themselves: a warp-collective operation between products stalls
+        // the issuing path while the tensor pipe runs dry.
+        if (lane == 0) {
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            return mbar_wait(bar, parity, abort, p.status, WAIT_LIMIT_NS);
+        };
         const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0) | (p.neg_a << 13);
         const uint32_t idesc_dp = idesc_bf16(128, 128, 0, 0);
         const uint32_t q_lo = desc_lo(sb + G::Q_OFF, 16), do_lo = desc_lo(sb + G::DO_OFF, 16);
         const uint32_t k_lo0 = desc_lo(sb + G::RING_OFF, 16), v_lo0 = desc_lo(sb + G::RING_OFF + G::TILE, 16);
-        bool ok = warp_wait(qd_full, 0, abort, p.status);
+        bool ok = wait(qd_full, 0);
         for (int j = 0; j < nj && ok; ++j) {
             const int st = j % NS;
             const uint32_t ph = (j / NS) & 1;
             const uint32_t so = (uint32_t)st * (G::STAGE >> 4);
-            if (!(ok = warp_wait(k_full(st), ph, abort, p.status))) break;
+            if (!(ok = wait(k_full(st), ph))) break;
             // The dS warps have read S_{j-1} and dP_{j-1}.
-            if (j > 0 && !(ok = warp_wait(s_free, (j - 1) & 1, abort, p.status))) break;
+            if (j > 0 && !(ok = wait(s_free, (j - 1) & 1))) break;
             tc_fence_after();
-            if (lane == 0) mma_k_is_d<D>(tmem + TM_S, q_lo, k_lo0 + so, idesc_s);      // S = Q K_j^T
-            __syncwarp();
-            if (!(ok = warp_wait(v_full(st), ph, abort, p.status))) break;
+            mma_k_is_d<D>(tmem + TM_S, q_lo, k_lo0 + so, idesc_s);      // S = Q K_j^T
+            if (!(ok = wait(v_full(st), ph))) break;
             tc_fence_after();
-            if (lane == 0) {
-                mma_k_is_d<D>(tmem + TM_DP, do_lo, v_lo0 + so, idesc_dp);              // dP = dO V_j^T
-                mma_commit(s_full);
-                mma_commit(kv_empty(st));
-            }
-            __syncwarp();
+            mma_k_is_d<D>(tmem + TM_DP, do_lo, v_lo0 + so, idesc_dp);              // dP = dO V_j^T
+            mma_commit(s_full);
+            mma_commit(kv_empty(st));
         }
         if (*abort) {
-            if (lane == 0) {
-                volatile int no_abort = 0;
-                mma_commit(drain(0));
-                mbar_wait(drain(0), 0, &no_abort, p.status, WAIT_LIMIT_NS);
-            }
-            __syncwarp();
+            volatile int no_abort = 0;
+            mma_commit(drain(0));
+            mbar_wait(drain(0), 0, &no_abort, p.status, WAIT_LIMIT_NS);
         }
+        }
+        __syncwarp();
     } else if (warp == DQ_WARP) {
         // ------------------------------------------------------------ dQ issuer
+        if (lane == 0) {
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            return mbar_wait(bar, parity, abort, p.status, WAIT_LIMIT_NS);
+        };
         const uint32_t k_mn_lo0 = desc_lo(sb + G::RING_OFF, 128 * 128);
         bool ok = true;
         for (int j = 0; j < nj && ok; ++j) {
@@ -255,26 +261,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_dq_tc_kernel(const __grid_con
             const uint32_t so = (uint32_t)st * (G::STAGE >> 4);
             // K_j cannot be refilled before this issuer's own commit below, so
             // its k_full phase is still the one of tile j.
-            if (!(ok = warp_wait(k_full(st), (j / NS) & 1, abort, p.status))) break;
-            if (!(ok = warp_wait(ds_full(b), (j >> 1) & 1, abort, p.status))) break;
+            if (!(ok = wait(k_full(st), (j / NS) & 1))) break;
+            if (!(ok = wait(ds_full(b), (j >> 1) & 1))) break;
             tc_fence_after();
-            if (lane == 0) {
 #pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks)                                    // dQ += dS K_j
-                    mma_n_is_d<D, true>(tmem + TM_DQ, tmem + TM_DS + 64u * b + 8u * ks, 0, k_mn_lo0 + so, ks, 0,
-                                        (j > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(ds_free(b));
-                mma_commit(kv_empty(st));
-            }
-            __syncwarp();
+            for (int ks = 0; ks < BK / 16; ++ks)                                    // dQ += dS K_j
+                mma_n_is_d<D, true>(tmem + TM_DQ, tmem + TM_DS + 64u * b + 8u * ks, 0, k_mn_lo0 + so, ks, 0,
+                                    (j > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(ds_free(b));
+            mma_commit(kv_empty(st));
         }
-        if (ok && lane == 0) mma_commit(dq_done);
+        if (ok) mma_commit(dq_done);
         if (*abort) {
-            if (lane == 0) {
-                volatile int no_abort = 0;
-                mma_commit(drain(1));
-                mbar_wait(drain(1), 0, &no_abort, p.status, WAIT_LIMIT_NS);
-            }
+            volatile int no_abort = 0;
+            mma_commit(drain(1));
+            mbar_wait(drain(1), 0, &no_abort, p.status, WAIT_LIMIT_NS);
+        }
         }
         __syncwarp();
     } else if (warp < 8) {

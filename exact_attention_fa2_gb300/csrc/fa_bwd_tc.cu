@@ -319,6 +319,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
+        // One thread runs this role from start to end, waiting on the
+        // barriers itself: no warp-collective operation between products
+        // (a shuffle or warp sync per wait measured ~300 cycles each on the
+        // issuing path, about as long as the products queued ahead of it).
+        if (lane == 0) {
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            return mbar_wait(bar, parity, abort, p.status, WAIT_LIMIT_NS);
+        };
         const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0) | (p.neg_a << 13);
         const uint32_t idesc_dp = idesc_bf16(128, 128, 0, 0);
         // Low descriptor words: K-major operands use LBO 16, the MN-major
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         const uint32_t ds_k_lo = desc_lo(sb + G::DS_OFF, 16);          // dS^T as K-major A (dK)
         const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);       // dS as M-major A (dQ)
         const uint32_t ds_hi = desc_hi(1024, SW_128B);
-        bool ok = warp_wait(kv_full, 0, abort, p.status);
+        bool ok = wait(kv_full, 0);
         if constexpr (TM::PIPE) {
             // S^T, dP^T of tile it+1 go in as soon as the softmax warps have
             // read those of tile it; dV, dK, dQ of tile it once P^T, dS^T exist.
@@ -341,56 +349,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);               // dP^T = V dO^T
                 mma_commit(s_full);
             };
-            if (ok) ok = warp_wait(q_full(0), 0, abort, p.status);
+            if (ok) ok = wait(q_full(0), 0);
             if (ok) {
                 tc_fence_after();
-                if (lane == 0) issue_sdp(0);
-                __syncwarp();
+                issue_sdp(0);
             }
             for (int it = 0; it < n_it && ok; ++it) {
                 const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
                 const uint32_t dso = (uint32_t)((it & 1) * G::DS_BYTES) >> 4;
                 if (it + 1 < n_it) {
-                    if (!(ok = warp_wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1, abort, p.status))) break;
-                    if (!(ok = warp_wait(s_free, it & 1, abort, p.status))) break;
+                    if (!(ok = wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1))) break;
+                    if (!(ok = wait(s_free, it & 1))) break;
                     tc_fence_after();
-                    if (lane == 0) issue_sdp(it + 1);
-                    __syncwarp();
+                    issue_sdp(it + 1);
                 }
-                if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
+                if (!(ok = wait(p_full, it & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
 #pragma unroll
-                    for (int ks = 0; ks < BQ / 16; ++ks)                                  // dV += P^T dO
-                        mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so, ks, 0,
-                                            (it > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(p_free);
+                for (int ks = 0; ks < BQ / 16; ++ks)                                  // dV += P^T dO
+                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so, ks, 0,
+                                        (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(p_free);
 #pragma unroll
-                    for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
-                        const uint64_t adesc =
-                            desc_make(ds_k_lo + dso + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                        mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
-                                             (it > 0 || ks > 0) ? 1u : 0u);
-                    }
-                    mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
-                    if constexpr (!WITH_DQ) mma_commit(ds_free(it & 1));   // dK has read dS^T
+                for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
+                    const uint64_t adesc =
+                        desc_make(ds_k_lo + dso + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
+                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
+                                         (it > 0 || ks > 0) ? 1u : 0u);
                 }
-                if constexpr (!WITH_DQ || TM::SPLIT_DQ) {
-                    // (d <= 32: dQ_i = dS K is issued by a thread of the dQ read-out warps.)
-                    __syncwarp();
-                    continue;
-                }
-                if (it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+                mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
+                if constexpr (!WITH_DQ) mma_commit(ds_free(it & 1));   // dK has read dS^T
+                // (d <= 32: dQ_i = dS K is issued by a thread of the dQ read-out warps.)
+                if constexpr (!WITH_DQ || TM::SPLIT_DQ) continue;
+                if (it > 0 && !(ok = wait(dq_empty, (it - 1) & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
-                        const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, ds_hi);
-                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
-                    }
-                    mma_commit(dq_full);
+                for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
+                    const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, ds_hi);
+                    mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
-                __syncwarp();
+                mma_commit(dq_full);
             }
         }
         if constexpr (!TM::PIPE) {
@@ -406,66 +404,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
                 mma_commit(s_full);
             };
-            if (ok) ok = warp_wait(q_full(0), 0, abort, p.status);
+            if (ok) ok = wait(q_full(0), 0);
             if (ok) {
                 tc_fence_after();
-                if (lane == 0) issue_s(0);
-                __syncwarp();
+                issue_s(0);
             }
             for (int it = 0; it < n_it && ok; ++it) {
                 const int s = it % NS;
                 const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
-                if (WITH_DQ && it > 0 && !(ok = warp_wait(dq_empty, (it - 1) & 1, abort, p.status))) break;
+                if (WITH_DQ && it > 0 && !(ok = wait(dq_empty, (it - 1) & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);             // dP^T = V dO^T
-                    mma_commit(dp_full);
-                }
-                if (!(ok = warp_wait(p_full, it & 1, abort, p.status))) break;
+                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
+                mma_commit(dp_full);
+                if (!(ok = wait(p_full, it & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
+                // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
 #pragma unroll
-                    for (int ks = 0; ks < BQ / 16; ++ks)
-                        mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
-                                            ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
-                }
-                __syncwarp();
-                if (!(ok = warp_wait(dst_full, it & 1, abort, p.status))) break;
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
+                                        ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                if (!(ok = wait(dst_full, it & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
 #pragma unroll
-                    for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
-                        const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                        mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
+                    const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
+                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                }
+                if constexpr (WITH_DQ) {
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
+                        const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
+                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                     }
-                    if constexpr (WITH_DQ) {
-#pragma unroll
-                        for (int ks = 0; ks < BK / 16; ++ks) {                              // dQ_i = dS K
-                            const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
-                            mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(dq_full);
-                    } else {
-                        mma_commit(q_empty(s));         // Q_i, dO_i (and L, D) are no longer read
-                    }
+                    mma_commit(dq_full);
+                } else {
+                    mma_commit(q_empty(s));         // Q_i, dO_i (and L, D) are no longer read
                 }
-                __syncwarp();
                 if (it + 1 < n_it) {
-                    if (!(ok = warp_wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1, abort, p.status))) break;
+                    if (!(ok = wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1))) break;
                     tc_fence_after();
-                    if (lane == 0) issue_s(it + 1);
-                    __syncwarp();
+                    issue_s(it + 1);
                 }
             }
         }
-        if (ok && lane == 0) mma_commit(done);
+        if (ok) mma_commit(done);
         if (*abort) {
-            if (lane == 0) {
-                volatile int no_abort = 0;
-                mma_commit(drain);
-                mbar_wait(drain, 0, &no_abort, p.status, WAIT_LIMIT_NS);
-            }
+            volatile int no_abort = 0;
+            mma_commit(drain);
+            mbar_wait(drain, 0, &no_abort, p.status, WAIT_LIMIT_NS);
+        }
         }
         __syncwarp();
     } else if (warp < DQ_WARP0) {

@@ -297,9 +297,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             }
             mma_commit(o_done(x));
         };
+        // One thread runs the issuer role from start to end and waits on the
+        // barriers itself: a warp-collective operation between products
+        // (a shuffle or warp sync per wait) stalls the issuing path for
+        // several hundred cycles, during which the tensor pipe runs dry.
+        if (lane == 0) {
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            return mbar_wait(bar, parity, abort, p.status, WAIT_LIMIT_NS);
+        };
         // Nothing to multiply when no key tile is admissible (partial attention).
-        bool ok = jB >= 0 && warp_wait(q_full, 0, abort, p.status);
-        if (ok) ok = warp_wait(k_full(0), 0, abort, p.status);
+        bool ok = jB >= 0 && wait(q_full, 0);
+        if (ok) ok = wait(k_full(0), 0);
         if constexpr (TM::PSEP) {
             // One issuer per tile; the next scores go in as soon as the
             // softmax has read these.
@@ -308,32 +316,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             if (jX < 0) ok = false;
             if (ok) {
                 tc_fence_after();
-                if (lane == 0) {
-                    issue_s(x, 0);
-                    mma_commit(k_empty(0));
-                }
-                __syncwarp();
+                issue_s(x, 0);
+                mma_commit(k_empty(0));
             }
             for (int j = 0; j <= jX && ok; ++j) {
                 const int st1 = (j + 1) % NS;
                 if (j + 1 <= jX) {
-                    if (!(ok = warp_wait(k_full(st1), ((j + 1) / NS) & 1, abort, p.status))) break;
-                    if (!(ok = warp_wait(s_free(x), j & 1, abort, p.status))) break;
+                    if (!(ok = wait(k_full(st1), ((j + 1) / NS) & 1))) break;
+                    if (!(ok = wait(s_free(x), j & 1))) break;
                     tc_fence_after();
-                    if (lane == 0) {
-                        issue_s(x, j + 1);
-                        mma_commit(k_empty(st1));
-                    }
-                    __syncwarp();
+                    issue_s(x, j + 1);
+                    mma_commit(k_empty(st1));
                 }
-                if (!(ok = warp_wait(v_full(j % NS), (j / NS) & 1, abort, p.status))) break;
-                if (!(ok = warp_wait(p_full(x), j & 1, abort, p.status))) break;
+                if (!(ok = wait(v_full(j % NS), (j / NS) & 1))) break;
+                if (!(ok = wait(p_full(x), j & 1))) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    issue_pv(x, j);
-                    mma_commit(v_empty(j % NS));
-                }
-                __syncwarp();
+                issue_pv(x, j);
+                mma_commit(v_empty(j % NS));
             }
         } else {
             // P_j sits in S_j's columns, so S_{j+1} follows P_j V_j.  One
@@ -342,45 +341,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             auto tile_has = [&](int x, int j) { return x == 0 ? j <= jA : (hasB && j <= jB); };
             if (ok) {
                 tc_fence_after();
-                if (lane == 0) {
-                    if (tile_has(0, 0)) issue_s(0, 0);
-                    if (tile_has(1, 0)) issue_s(1, 0);
-                    mma_commit(k_empty(0));
-                }
-                __syncwarp();
+                if (tile_has(0, 0)) issue_s(0, 0);
+                if (tile_has(1, 0)) issue_s(1, 0);
+                mma_commit(k_empty(0));
             }
             for (int j = 0; j <= jB && ok; ++j) {
                 const bool next = j + 1 <= jB;
                 const int st1 = (j + 1) % NS;
-                if (!(ok = warp_wait(v_full(j % NS), (j / NS) & 1, abort, p.status))) break;
-                if (next && !(ok = warp_wait(k_full(st1), ((j + 1) / NS) & 1, abort, p.status))) break;
+                if (!(ok = wait(v_full(j % NS), (j / NS) & 1))) break;
+                if (next && !(ok = wait(k_full(st1), ((j + 1) / NS) & 1))) break;
                 for (int x = 0; x < 2 && ok; ++x) {
                     if (!tile_has(x, j)) continue;
-                    if (!(ok = warp_wait(p_full(x), j & 1, abort, p.status))) break;
+                    if (!(ok = wait(p_full(x), j & 1))) break;
                     tc_fence_after();
-                    if (lane == 0) {
-                        issue_pv(x, j);
-                        if (tile_has(x, j + 1)) issue_s(x, j + 1);
-                    }
-                    __syncwarp();
+                    issue_pv(x, j);
+                    if (tile_has(x, j + 1)) issue_s(x, j + 1);
                 }
                 if (!ok) break;
-                if (lane == 0) {
-                    mma_commit(v_empty(j % NS));
-                    if (next) mma_commit(k_empty(st1));
-                }
-                __syncwarp();
+                mma_commit(v_empty(j % NS));
+                if (next) mma_commit(k_empty(st1));
             }
         }
         if (*abort) {
             // Wait until every MMA this thread issued has finished before TMEM is freed.
-            if (lane == 0) {
-                volatile int no_abort = 0;
-                mma_commit(drain(warp - MMA_WARP));
-                mbar_wait(drain(warp - MMA_WARP), 0, &no_abort, p.status, WAIT_LIMIT_NS);
-            }
-            __syncwarp();
+            volatile int no_abort = 0;
+            mma_commit(drain(warp - MMA_WARP));
+            mbar_wait(drain(warp - MMA_WARP), 0, &no_abort, p.status, WAIT_LIMIT_NS);
         }
+        }
+        __syncwarp();
     } else if (warp < 4 || (warp < 8 && hasB)) {
         // ------------------------------------------------------------ softmax + epilogue of tile x
         const int x = warp >> 2;

@@ -48,31 +48,34 @@ def _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=None):
     return dq, dk, dv
 
 
+def _check_case(lib, shape, dtype, causal, seed):
+    B, H, S, d = shape
+    q, k, v, do = (t.to(DEV) for t in make_inputs(B, H, S, d, dtype, seed=seed))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, causal, scale)
+    ref = fa.bwd(q, k, v, o, do, lse, causal, scale)
+    outs = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
+    # The first call on the device looks up the scratch's address; from then
+    # on a call changes neither PyTorch's allocations nor the device's free
+    # memory.
+    _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[0])
+    torch.cuda.synchronize()
+    before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+    _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[1])
+    torch.cuda.synchronize()
+    assert (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]) == before
+    # dK and dV come from the same deterministic kernels on both calls.
+    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
+    for call, got in enumerate(outs):
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            assert_close(f"{name} {dtype} (call {call + 1})", a.cpu(), b.cpu(), *TOL[dtype]["grad"])
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row():
     lib = _lib()
-    cases = [((2, 4, 1024, 64), "bf16", True, 9001), ((1, 2, 333, 80), "fp32", False, 9002)]
-    for (B, H, S, d), dtype, causal, seed in cases:
-        q, k, v, do = (t.to(DEV) for t in make_inputs(B, H, S, d, dtype, seed=seed))
-        scale = 1.0 / math.sqrt(d)
-        o, lse = fa.fwd(q, k, v, causal, scale)
-        ref = fa.bwd(q, k, v, o, do, lse, causal, scale)
-        outs = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
-        # The first call on the device looks up the scratch's address; from
-        # then on a call changes neither PyTorch's allocations nor the
-        # device's free memory.
-        _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[0])
-        torch.cuda.synchronize()
-        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
-        got = _noalloc_bwd(lib, q, k, v, o, do, lse, causal, scale, out=outs[1])
-        torch.cuda.synchronize()
-        assert (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]) == before
-        # dK and dV come from the same deterministic kernels on both calls.
-        assert torch.equal(outs[0][1], got[1]) and torch.equal(outs[0][2], got[2])
-        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
-            assert_close(f"{name} {dtype}", a.cpu(), b.cpu(), *TOL[dtype]["grad"])
-        for name, a, b in zip(("dq", "dk", "dv"), outs[0], ref):
-            assert_close(f"{name} {dtype} (first call)", a.cpu(), b.cpu(), *TOL[dtype]["grad"])
+    _check_case(lib, (2, 4, 1024, 64), "bf16", True, 9001)
+    _check_case(lib, (1, 2, 333, 80), "fp32", False, 9002)
 
 
 @pytest.mark.gpu
