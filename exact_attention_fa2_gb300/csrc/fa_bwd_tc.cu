@@ -219,9 +219,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
         mbar_init(kv_full, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(q_full(s), 33);        // TMA expect-tx arrival + 32 lanes that stage (L, D)
-            // d <= 64: the MMA issuer once dV and dK (the last readers) are issued;
-            // otherwise the dQ warpgroup, once the dQ_i staged in the slot has been read.
-            mbar_init(q_empty(s), 1);
+            // The slot is free once its last readers are done: dV and dK (the
+            // MMA issuer's commit) and, where dQ_i is staged in it, the dQ
+            // reduce-add's read (d = 64: both; d > 64: the reduce alone, whose
+            // dQ_i follows dK on the same issuer; d <= 32 and the dK/dV-only
+            // backward: the issuer alone).
+            mbar_init(q_empty(s), (WITH_DQ && TM::PIPE && !TM::SPLIT_DQ) ? 2 : 1);
         }
         mbar_init(s_full, 1);
         mbar_init(p_full, 2 * BK);
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(dq_full);
+                mma_commit(ds_free(it & 1));        // dK and dQ_i have read dS^T
             }
         }
         if constexpr (!TM::PIPE) {
@@ -683,11 +687,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
             // the tile is staged over it; its commit completes q_empty.
             if (TM::SPLIT_DQ && !warp_wait(q_empty(s), (it / NS) & 1, abort, p.status)) break;
             tc_fence_after();
-            // Stage this row box by box in the TMA swizzle: for d <= 64 into
-            // the dS^T buffer that dK and dQ_i have just read (dQ_i is 32 KB
-            // at most), otherwise into the Q_i / dO_i slot (the products that
-            // read them finished before dQ_i did).
-            const uint32_t slot = TM::PIPE ? sb + G::DS_OFF + (uint32_t)((it & 1) * G::DS_BYTES) : q_slot(s);
+            // Stage this row box by box in the TMA swizzle: for d <= 32 into
+            // the dS^T buffer that dK and dQ_i have just read, otherwise into
+            // the Q_i / dO_i slot, whose readers finished before dQ_i did (the
+            // dS^T buffer is then released by the issuer as soon as dQ_i has
+            // read it, instead of after the reduce-add's slow read).
+            constexpr bool IN_DS = TM::PIPE && TM::SPLIT_DQ;
+            const uint32_t slot = IN_DS ? sb + G::DS_OFF + (uint32_t)((it & 1) * G::DS_BYTES) : q_slot(s);
 #pragma unroll
             for (int cq = 0; cq < QC::NCH; ++cq) {
                 constexpr int W32 = 32;
@@ -725,7 +731,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                     bulk_commit();
                     bulk_wait_read();
                     // The buffer may take the next dS^T / the next Q, dO tile.
-                    mbar_arrive(TM::PIPE ? ds_free(it & 1) : q_empty(s));
+                    mbar_arrive(IN_DS ? ds_free(it & 1) : q_empty(s));
                 } else {
                     lead_ok = 0;
                 }

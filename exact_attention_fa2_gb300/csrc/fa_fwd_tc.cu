@@ -435,7 +435,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
                 exp_pairs(r + 64 * half, c2, n2, pk, sum);
                 // The previous product P_{j-1} V_{j-1} must have finished: it
                 // read the P columns and it wrote the O rescaled below.
-                if (half == 0 && j > 0) {
+                // d > 64: S_j's commit follows P_{j-1} V_{j-1} on the same issuer, so
+                // s_full already implies it; d <= 64 issues S_j ahead of it.
+                if (TM::PSEP && half == 0 && j > 0) {
                     if (!(ok = warp_wait(o_done(x), (j - 1) & 1, abort, p.status))) break;
                     tc_fence_after();
                 }
@@ -449,21 +451,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
             f2unpack(sum[3], s6, s7);
             l_sum = l_sum * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // O *= alpha, up to 64 columns per Tensor Memory round trip.
                 const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
-                for (int u = 0; u < D / 16; ++u) {
-                    uint32_t o[16];
-                    tmem_ld16(tO + 16 * u, o);
-                    tmem_wait_ld();
-                    reg_fence<16>(o);
+                for (int u0 = 0; u0 < D / 16; u0 += 4) {
+                    constexpr int NB = 4;
+                    uint32_t o[16 * NB];
 #pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
+                    for (int u = 0; u < NB; ++u)
+                        if (u0 + u < D / 16) tmem_ld16(tO + 16 * (u0 + u), o + 16 * u);
+                    tmem_wait_ld();
+                    reg_fence<16 * NB>(o);
+#pragma unroll
+                    for (int i = 0; i < 16 * NB; i += 2) {
                         float lo, hi;
                         f2unpack(mul2(f2pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
                         o[i] = __float_as_uint(lo);
                         o[i + 1] = __float_as_uint(hi);
                     }
-                    tmem_st16(tO + 16 * u, o);
+#pragma unroll
+                    for (int u = 0; u < NB; ++u)
+                        if (u0 + u < D / 16) tmem_st16(tO + 16 * (u0 + u), o + 16 * u);
                 }
             }
             tmem_wait_st();
