@@ -23,7 +23,8 @@
 // query columns 0-63, warps 4-7 columns 64-127) and the final dK/dV store,
 // warps 8-11 the dQ read-out (one thread per query row), warp 12 TMA (K, V
 // once; Q_i, dO_i per tile, plus L and D), warp 13 Tensor Memory allocation
-// and the single-thread MMA issuer.
+// and one thread that issues the products (for d = 64 it issues S^T and dP^T
+// only, and a thread of warp 14 issues dV, dK and dQ_i).
 // Tensor Memory columns: dV [0,128), dK [128,256), S^T/P^T [256,384),
 // dP^T [384,512), which dQ_i reuses once dS^T has been formed.  With this
 // layout (d > 64) the products of tile i are issued as S^T; dP^T once dQ_{i-1}
@@ -49,10 +50,14 @@ using namespace tc;
 
 constexpr int BK = 128;
 constexpr int BQ = 128;
-constexpr int NTHREADS = 448;
+
 constexpr int DQ_WARP0 = 8;
 constexpr int TMA_WARP = 12;
 constexpr int MMA_WARP = 13;
+constexpr int MMA_WARP2 = 14;      // d = 64: second issuer (dV, dK, dQ_i)
+// Threads per CTA: 14 warps, plus warp MMA_WARP2 where it issues (d = 64).
+template <int D>
+constexpr int bwd_threads() { return (D > 32 && D <= 64) ? 480 : 448; }
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 256, TM_DP = 384;
 constexpr int SMEM_BUDGET = 227 * 1024;
@@ -158,7 +163,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // a separate query-tile-outer pass); the dQ warps then stay idle and the
 // buffers the dQ read-out would release are released by the MMA issuer.
 template <int D, bool WITH_DQ>
-__global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
     using C = Chunks<D>;
     using QC = DqChunks<D>;
     using G = BwdCfg<D>;
@@ -320,13 +325,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mbar_wait(q_full(it % NS), (it / NS) & 1, &no_abort, p.status, WAIT_LIMIT_NS);
         }
         __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == MMA_WARP || warp == MMA_WARP2) {
+        // ------------------------------------------------------------ MMA issuers
         // One thread runs this role from start to end, waiting on the
         // barriers itself: no warp-collective operation between products
         // (a shuffle or warp sync per wait measured ~300 cycles each on the
         // issuing path, about as long as the products queued ahead of it).
-        if (lane == 0) {
+        constexpr bool TWO = TM::PIPE && !TM::SPLIT_DQ;
+        if (lane == 0 && (warp == MMA_WARP || TWO)) {
         auto wait = [&](uint32_t bar, uint32_t parity) {
             return mbar_wait(bar, parity, abort, p.status, WAIT_LIMIT_NS);
         };
@@ -352,20 +358,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);               // dP^T = V dO^T
                 mma_commit(s_full);
             };
-            if (ok) ok = wait(q_full(0), 0);
-            if (ok) {
-                tc_fence_after();
-                issue_sdp(0);
+            // d = 64: S^T, dP^T on this thread (warp MMA_WARP), dV, dK, dQ_i on
+            // warp MMA_WARP2's: the next scores go in as soon as the softmax
+            // has read these, whatever the other products are waiting for.
+            const bool do_sdp = !TWO || warp == MMA_WARP;
+            const bool do_rest = !TWO || warp == MMA_WARP2;
+            if (do_sdp) {
+                if (ok) ok = wait(q_full(0), 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sdp(0);
+                }
             }
             for (int it = 0; it < n_it && ok; ++it) {
                 const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
                 const uint32_t dso = (uint32_t)((it & 1) * G::DS_BYTES) >> 4;
-                if (it + 1 < n_it) {
+                if (do_sdp && it + 1 < n_it) {
                     if (!(ok = wait(q_full((it + 1) % NS), ((it + 1) / NS) & 1))) break;
                     if (!(ok = wait(s_free, it & 1))) break;
                     tc_fence_after();
                     issue_sdp(it + 1);
                 }
+                if (!do_rest) continue;
                 if (!(ok = wait(p_full, it & 1))) break;
                 tc_fence_after();
 #pragma unroll
@@ -451,11 +465,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_tc_kernel(const __grid_consta
                 }
             }
         }
-        if (ok) mma_commit(done);
+        if (ok && (!TWO || warp == MMA_WARP2)) mma_commit(done);
         if (*abort) {
+            // Every product this thread issued has finished before TMEM is freed.
             volatile int no_abort = 0;
-            mma_commit(drain);
-            mbar_wait(drain, 0, &no_abort, p.status, WAIT_LIMIT_NS);
+            const uint32_t dr = warp == MMA_WARP ? drain : drain_dq;
+            mma_commit(dr);
+            mbar_wait(dr, 0, &no_abort, p.status, WAIT_LIMIT_NS);
         }
         }
         __syncwarp();
@@ -811,7 +827,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     auto kern = bwd_tc_kernel<D, WITH_DQ>;
     cudaError_t e = set_smem_limit<bwd_tc_kernel<D, WITH_DQ>>(G::DYN_SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(p.n_kv * BH), dim3(NTHREADS), G::DYN_SMEM, a.stream, p);
+    return launch_pdl(kern, dim3(p.n_kv * BH), dim3(bwd_threads<D>()), G::DYN_SMEM, a.stream, p);
 }
 
 template <bool WITH_DQ>
