@@ -240,10 +240,19 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ our arm
+def sources_sha16(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the listed files, concatenated in
+    order (a kernel source and the headers it includes)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel_name: str, workload_name: str):
     """DRAM bytes per launch from a committed ncu summary, only if the kernel
-    source it was taken from is unchanged."""
-    import hashlib
+    source and the headers it was built from are unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -252,9 +261,8 @@ def load_traffic(kernel_name: str, workload_name: str):
         ent = j.get(kernel_name, {}).get(workload_name)
         if not ent:
             return None
-        src = os.path.join(ROOT, ent["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return ent["dram_bytes_per_launch"] if sha == ent["source_sha256_16"] else None
+        paths = ent["sources"] if "sources" in ent else [ent["source"]]
+        return ent["dram_bytes_per_launch"] if sources_sha16(paths) == ent["source_sha256_16"] else None
     except Exception:
         return None
 

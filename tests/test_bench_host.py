@@ -94,12 +94,27 @@ def test_traffic_used_only_while_the_source_is_unchanged(bench, tmp_path, monkey
     assert bench.load_traffic("k", "c2") is None                          # stale figure dropped
 
 
+def test_traffic_record_covers_the_included_headers(bench, tmp_path, monkeypatch):
+    """A figure is dropped when a header the kernel includes changes, not only its .cu file."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "k.cu").write_bytes(b"#include \"h.cuh\"\n")
+    (tmp_path / "h.cuh").write_bytes(b"// v1\n")
+    (tmp_path / "profiles").mkdir()
+    rec = {"k": {"c4": {"sources": ["k.cu", "h.cuh"], "source_sha256_16": bench.sources_sha16(["k.cu", "h.cuh"]),
+                        "dram_bytes_per_launch": 99}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.load_traffic("k", "c4") == 99
+    (tmp_path / "h.cuh").write_bytes(b"// v2\n")
+    assert bench.load_traffic("k", "c4") is None
+
+
 def test_committed_traffic_record_is_well_formed():
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     assert rec, "empty traffic record"
     for kern, by_workload in rec.items():
         for wl, ent in by_workload.items():
-            assert os.path.exists(os.path.join(ROOT, ent["source"])), (kern, wl)
+            for src in ent.get("sources", [ent.get("source")]):
+                assert src and os.path.exists(os.path.join(ROOT, src)), (kern, wl)
             assert os.path.exists(os.path.join(ROOT, ent["from"])), (kern, wl)
             assert len(ent["source_sha256_16"]) == 16
             assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
