@@ -41,6 +41,7 @@
 #include "fa_tc_common.cuh"
 
 #include <cstring>
+#include <type_traits>
 
 namespace fa {
 namespace {
@@ -84,9 +85,17 @@ struct BwdTm {
     __device__ static constexpr uint32_t p_kstep(int ks) { return PIPE ? P + 8 * ks : P + (ks / 4) * 64 + (ks % 4) * 8; }
 };
 
+// Head-dim layout of the K, V, Q, dO tiles.  d = 80 uses unpadded 16-column
+// chunks: the padded layout makes the tensor cores read (and the TMA write) a
+// 64-column remainder box for 16 columns, and 20 KB tiles leave room for three
+// [Q_i | dO_i] stages instead of two (each slot still takes the staged fp32
+// dQ_i, 40 KB).
+template <int D>
+using BwdChunks = std::conditional_t<D == 80, ChunksW<D, 16>, Chunks<D>>;
+
 template <int D>
 struct BwdCfg {
-    static constexpr int TILE = Chunks<D>::tile_bytes(128);
+    static constexpr int TILE = BwdChunks<D>::tile_bytes(128);
     static constexpr int DS_BYTES = BK * BQ * 2;
     static constexpr int NDS = BwdTm<D>::PIPE ? 2 : 1;      // dS^T buffers
     static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
@@ -113,8 +122,9 @@ struct BwdCfg {
 
 // fp32 dQ tile [128 rows][d] staged for TMA as 32-column boxes (128-byte
 // rows, 128-byte swizzle) plus one 16-column box (64-byte rows, 64-byte
-// swizzle) when d is not a multiple of 32.  128 * d * 4 bytes = the Q_i + dO_i
-// slot it is staged in.
+// swizzle) when d is not a multiple of 32.  For d > 64 it is staged in the
+// Q_i + dO_i slot (2 x 32 KB padded tiles, 2 x 20 KB for d = 80), for d <= 64
+// in the slot or in a dS^T buffer.
 template <int D>
 struct DqChunks {
     static constexpr int N32 = D / 32;
@@ -122,6 +132,8 @@ struct DqChunks {
     __host__ __device__ static constexpr int width(int c) { return c < N32 ? 32 : 16; }
     __host__ __device__ static constexpr int map_index(int c) { return c < N32 ? 0 : 1; }
     __host__ __device__ static constexpr int offset(int c) { return c * 128 * 128; }
+    static constexpr int SPAN = offset(NCH - 1) + 128 * width(NCH - 1) * 4;
+    static_assert(SPAN <= 2 * BwdCfg<D>::TILE, "staged dQ tile fits a Q_i + dO_i slot");
 };
 
 struct BwdParams {
@@ -164,7 +176,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // buffers the dQ read-out would release are released by the MMA issuer.
 template <int D, bool WITH_DQ>
 __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __grid_constant__ BwdParams p) {
-    using C = Chunks<D>;
+    using C = BwdChunks<D>;
     using QC = DqChunks<D>;
     using G = BwdCfg<D>;
     constexpr int NS = G::NS;
@@ -272,10 +284,10 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
             mbar_arrive_expect_tx(kv_full, 2 * G::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-                tma_load_view(sb + G::K_OFF + C::tile_off(c, BK), &p.tk[C::map_index(c)], p.map3 & 2u, c * 64, k0, hh,
-                              bb, bh, kv_full);
-                tma_load_view(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], p.map3 & 4u, c * 64, k0, hh,
-                              bb, bh, kv_full);
+                tma_load_view(sb + G::K_OFF + C::tile_off(c, BK), &p.tk[C::map_index(c)], p.map3 & 2u, C::col(c), k0,
+                              hh, bb, bh, kv_full);
+                tma_load_view(sb + G::V_OFF + C::tile_off(c, BK), &p.tv[C::map_index(c)], p.map3 & 4u, C::col(c), k0,
+                              hh, bb, bh, kv_full);
             }
         }
         const size_t rb = (size_t)bh * S;
@@ -300,10 +312,10 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 mbar_arrive_expect_tx(q_full(s), 2 * G::TILE);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_view(q_slot(s) + C::tile_off(c, BQ), &p.tq[C::map_index(c)], p.map3 & 1u, c * 64, q0, hh,
-                                  bb, bh, q_full(s));
-                    tma_load_view(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], p.map3 & 8u, c * 64, q0, hh,
-                                  bb, bh, q_full(s));
+                    tma_load_view(q_slot(s) + C::tile_off(c, BQ), &p.tq[C::map_index(c)], p.map3 & 1u, C::col(c), q0,
+                                  hh, bb, bh, q_full(s));
+                    tma_load_view(do_slot(s) + C::tile_off(c, BQ), &p.tdo[C::map_index(c)], p.map3 & 8u, C::col(c), q0,
+                                  hh, bb, bh, q_full(s));
                 }
             }
             // Stored per pair of rows (2r, 2r+1) as (-L2_2r, -L2_2r+1, -D_2r,
@@ -339,12 +351,13 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
         const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0) | (p.neg_a << 13);
         const uint32_t idesc_dp = idesc_bf16(128, 128, 0, 0);
         // Low descriptor words: K-major operands use LBO 16, the MN-major
-        // [rows][d] tiles use the 64-column chunk stride as LBO.
+        // [rows][d] tiles use the head-dim chunk stride as LBO.
+        constexpr uint32_t CH = C::tile_off(1, 128);
         const uint32_t k_lo = desc_lo(sb + G::K_OFF, 16), v_lo = desc_lo(sb + G::V_OFF, 16);
-        const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, 128 * 128);
+        const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, CH);
         const uint32_t q_lo0 = desc_lo(sb + G::QD_OFF, 16), do_lo0 = desc_lo(sb + G::QD_OFF + G::TILE, 16);
-        const uint32_t q_mn_lo0 = desc_lo(sb + G::QD_OFF, 128 * 128);
-        const uint32_t do_mn_lo0 = desc_lo(sb + G::QD_OFF + G::TILE, 128 * 128);
+        const uint32_t q_mn_lo0 = desc_lo(sb + G::QD_OFF, CH);
+        const uint32_t do_mn_lo0 = desc_lo(sb + G::QD_OFF + G::TILE, CH);
         const uint32_t ds_k_lo = desc_lo(sb + G::DS_OFF, 16);          // dS^T as K-major A (dK)
         const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);       // dS as M-major A (dQ)
         const uint32_t ds_hi = desc_hi(1024, SW_128B);
@@ -354,8 +367,8 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
             // read those of tile it; dV, dK, dQ of tile it once P^T, dS^T exist.
             auto issue_sdp = [&](int it) {
                 const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
-                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
-                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);               // dP^T = V dO^T
+                mma_k_is_d<D, C>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
+                mma_k_is_d<D, C>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);               // dP^T = V dO^T
                 mma_commit(s_full);
             };
             // d = 64: S^T, dP^T on this thread (warp MMA_WARP), dV, dK, dQ_i on
@@ -384,14 +397,14 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)                                  // dV += P^T dO
-                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so, ks, 0,
+                    mma_n_is_d<D, true, C>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so, ks, 0,
                                         (it > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(p_free);
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks) {                                  // dK += dS^T Q
                     const uint64_t adesc =
                         desc_make(ds_k_lo + dso + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
+                    mma_n_is_d<D, false, C>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0,
                                          (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 mma_commit(q_empty(it % NS));       // Q_i, dO_i (and L, D) are no longer read
@@ -403,7 +416,7 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
 #pragma unroll
                 for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
                     const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                    mma_n_is_d<D, false, C>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(dq_full);
                 mma_commit(ds_free(it & 1));        // dK and dQ_i have read dS^T
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
             // read the one dS^T buffer.
             auto issue_s = [&](int it) {
                 const uint32_t so = (uint32_t)(it % NS) * ((2 * G::TILE) >> 4);
-                mma_k_is_d<D>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
+                mma_k_is_d<D, C>(tmem + TM_S, k_lo, q_lo0 + so, idesc_s);                  // S^T = K Q^T
                 mma_commit(s_full);
             };
             if (ok) ok = wait(q_full(0), 0);
@@ -432,27 +445,27 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 const uint32_t so = (uint32_t)s * ((2 * G::TILE) >> 4);
                 if (WITH_DQ && it > 0 && !(ok = wait(dq_empty, (it - 1) & 1))) break;
                 tc_fence_after();
-                mma_k_is_d<D>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
+                mma_k_is_d<D, C>(tmem + TM_DP, v_lo, do_lo0 + so, idesc_dp);                 // dP^T = V dO^T
                 mma_commit(dp_full);
                 if (!(ok = wait(p_full, it & 1))) break;
                 tc_fence_after();
                 // dV += P^T dO: P^T of query columns 64h.. sits at TMEM columns 64h.. of S^T.
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks)
-                    mma_n_is_d<D, true>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
+                    mma_n_is_d<D, true, C>(tmem + TM::DV, tmem + TM::p_kstep(ks), 0, do_mn_lo0 + so,
                                         ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                 if (!(ok = wait(dst_full, it & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < BQ / 16; ++ks) {                                      // dK += dS^T Q
                     const uint64_t adesc = desc_make(ds_k_lo + (((ks / 4) * 16384 + (ks % 4) * 32) >> 4), ds_hi);
-                    mma_n_is_d<D, false>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
+                    mma_n_is_d<D, false, C>(tmem + TM::DK, 0, adesc, q_mn_lo0 + so, ks, 0, (it > 0 || ks > 0) ? 1u : 0u);
                 }
                 if constexpr (WITH_DQ) {
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
                         const uint64_t adesc = desc_make(ds_m_lo + ks * 128, ds_hi);
-                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                        mma_n_is_d<D, false, C>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(dq_full);
                 } else {
@@ -687,12 +700,12 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t dso = (uint32_t)((it & 1) * G::DS_BYTES) >> 4;
-                    const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, 128 * 128);
+                    const uint32_t k_mn_lo = desc_lo(sb + G::K_OFF, C::tile_off(1, 128));
                     const uint32_t ds_m_lo = desc_lo(sb + G::DS_OFF, 16384);
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks) {                                  // dQ_i = dS K
                         const uint64_t adesc = desc_make(ds_m_lo + dso + ks * 128, desc_hi(1024, SW_128B));
-                        mma_n_is_d<D, false>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
+                        mma_n_is_d<D, false, C>(tmem + TM::DQ, 0, adesc, k_mn_lo, ks, 1, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(dq_full);
                 }
@@ -775,7 +788,7 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
 
 template <int D, bool WITH_DQ>
 cudaError_t bwd_tc_launch(const BwdArgs& a) {
-    using C = Chunks<D>;
+    using C = BwdChunks<D>;
     using G = BwdCfg<D>;
     BwdParams p;
     memset(&p, 0, sizeof(p));
@@ -787,11 +800,12 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     for (int i = 0; i < 4; ++i) {
         cudaError_t e;
         bool r3 = false;
-        if (C::N64 > 0 &&
-            (e = make_tmap_bf16_view(&maps[i][0], &r3, src[i], D, rows[i], a.H, a.B, views[i], 64, 128)) != cudaSuccess)
+        if (C::MAP_W0 > 0 &&
+            (e = make_tmap_bf16_view(&maps[i][0], &r3, src[i], D, rows[i], a.H, a.B, views[i], C::MAP_W0, 128)) !=
+                cudaSuccess)
             return e;
-        if (C::REM > 0 && !C::PAD &&
-            (e = make_tmap_bf16_view(&maps[i][1], &r3, src[i], D, rows[i], a.H, a.B, views[i], C::REM, 128)) !=
+        if (C::MAP_W1 > 0 &&
+            (e = make_tmap_bf16_view(&maps[i][1], &r3, src[i], D, rows[i], a.H, a.B, views[i], C::MAP_W1, 128)) !=
                 cudaSuccess)
             return e;
         if (r3) p.map3 |= 1u << i;

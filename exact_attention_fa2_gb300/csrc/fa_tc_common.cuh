@@ -35,8 +35,33 @@ struct Chunks {
     }
     __host__ __device__ static constexpr int row_bytes(int c) { return PAD ? 128 : width(c) * 2; }
     __host__ __device__ static constexpr int map_index(int c) { return (PAD || width(c) == 64) ? 0 : 1; }
+    __host__ __device__ static constexpr int col(int c) { return 64 * c; }
+    // Box widths of the two TMA maps (0: map unused).
+    static constexpr int MAP_W0 = N64 > 0 ? 64 : 0;
+    static constexpr int MAP_W1 = (REM > 0 && !PAD) ? REM : 0;
     // One instruction covers N = d for the products whose N is the head dim.
     static constexpr bool SINGLE_N = D == 128 || PAD;
+};
+
+// The head dimension in W-column chunks (W = 16: 32-byte rows and swizzle;
+// W = 32: 64-byte), unpadded: a d = 80 tile of 128 rows takes 20 KB with
+// W = 16 instead of the padded 32 KB.  The chunks are uniform, so a product
+// whose N is the head dim is still one instruction (N-direction atoms of W
+// columns, one chunk apart), and a k-step over d stays inside one chunk.
+template <int D, int W>
+struct ChunksW {
+    static_assert((W == 16 || W == 32) && D % W == 0, "uniform 16- or 32-column chunks");
+    static constexpr int NCH = D / W;
+    __host__ __device__ static constexpr int width(int) { return W; }
+    __host__ __device__ static constexpr int col(int c) { return W * c; }
+    __host__ __device__ static constexpr int tile_off(int c, int rows) { return c * rows * W * 2; }
+    __host__ __device__ static constexpr int tile_bytes(int rows) { return rows * D * 2; }
+    __host__ __device__ static constexpr uint32_t swz(int) { return W == 16 ? SW_32B : SW_64B; }
+    __host__ __device__ static constexpr int row_bytes(int) { return W * 2; }
+    __host__ __device__ static constexpr int map_index(int) { return 1; }
+    static constexpr int MAP_W0 = 0;
+    static constexpr int MAP_W1 = W;
+    static constexpr bool SINGLE_N = true;
 };
 
 // Block b of a flat grid of n_units units for each of BH heads, ordered in
@@ -89,16 +114,16 @@ __device__ __forceinline__ void reg_fence(uint32_t* r) {
 }
 
 // B operand of the products whose N dimension is the head dim: a [rows][d]
-// tile (TMA layout, 128 rows) read MN-major, k-step of 16 rows `ks`.
-// `b_lo` is the low descriptor word of the tile (LBO = the 64-column chunk
+// tile (TMA layout, 128 rows, chunked as C) read MN-major, k-step of 16 rows
+// `ks`.  `b_lo` is the low descriptor word of the tile (LBO = the chunk
 // stride); the A operand is either Tensor Memory (`a_tm`) or shared memory
 // (`a_desc`).
-template <int D, bool A_TMEM>
+template <int D, bool A_TMEM, class C = Chunks<D>>
 __device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint64_t a_desc, uint32_t b_lo, int ks,
                                            uint32_t a_mn, uint32_t acc) {
-    using C = Chunks<D>;
     if constexpr (C::SINGLE_N) {
-        const uint64_t bdesc = desc_make(b_lo + ks * 128, desc_hi(1024, SW_128B));
+        const uint64_t bdesc =
+            desc_make(b_lo + ((ks * 16 * C::row_bytes(0)) >> 4), desc_hi(8 * C::row_bytes(0), C::swz(0)));
         if constexpr (A_TMEM) mma_ts(d_tmem, a_tm, bdesc, idesc_bf16(128, D, 0, 1), acc);
         else mma_ss(d_tmem, a_desc, bdesc, idesc_bf16(128, D, a_mn, 1), acc);
     } else {
@@ -113,10 +138,10 @@ __device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint32_t a_tm, uint6
 }
 
 // C[128x128] = A[128 x d] B[128 x d]^T with both tiles K-major (head dim
-// contiguous); a_lo / b_lo are the tiles' low descriptor words (LBO 16).
-template <int D>
+// contiguous, chunked as C); a_lo / b_lo are the tiles' low descriptor words
+// (LBO 16).
+template <int D, class C = Chunks<D>>
 __device__ __forceinline__ void mma_k_is_d(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
-    using C = Chunks<D>;
     int step = 0;
 #pragma unroll
     for (int c = 0; c < C::NCH; ++c) {
