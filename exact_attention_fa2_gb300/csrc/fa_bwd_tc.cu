@@ -85,13 +85,15 @@ struct BwdTm {
     __device__ static constexpr uint32_t p_kstep(int ks) { return PIPE ? P + 8 * ks : P + (ks / 4) * 64 + (ks % 4) * 8; }
 };
 
-// Head-dim layout of the K, V, Q, dO tiles.  d = 80 uses unpadded 16-column
-// chunks: the padded layout makes the tensor cores read (and the TMA write) a
-// 64-column remainder box for 16 columns, and 20 KB tiles leave room for three
-// [Q_i | dO_i] stages instead of two (each slot still takes the staged fp32
-// dQ_i, 40 KB).
+// Head-dim layout of the K, V, Q, dO tiles.  64-column chunks pad d = 80 and
+// 96 to 128 columns: the tensor cores then read (and the TMA writes) a
+// 64-column remainder box for 16 or 32 columns.  d = 80 uses unpadded
+// 16-column chunks instead: 20 KB tiles leave room for three [Q_i | dO_i]
+// stages instead of two (each slot still takes the staged fp32 dQ_i, 40 KB).
+// d = 96 uses unpadded 32-column chunks (24 KB tiles, still two stages;
+// 16-column chunks of the same size measured slower).
 template <int D>
-using BwdChunks = std::conditional_t<D == 80, ChunksW<D, 16>, Chunks<D>>;
+using BwdChunks = std::conditional_t<D == 80, ChunksW<D, 16>, std::conditional_t<D == 96, ChunksW<D, 32>, Chunks<D>>>;
 
 template <int D>
 struct BwdCfg {
@@ -123,8 +125,8 @@ struct BwdCfg {
 // fp32 dQ tile [128 rows][d] staged for TMA as 32-column boxes (128-byte
 // rows, 128-byte swizzle) plus one 16-column box (64-byte rows, 64-byte
 // swizzle) when d is not a multiple of 32.  For d > 64 it is staged in the
-// Q_i + dO_i slot (2 x 32 KB padded tiles, 2 x 20 KB for d = 80), for d <= 64
-// in the slot or in a dS^T buffer.
+// Q_i + dO_i slot (2 x 32 KB tiles for d = 128, 2 x 24 KB for d = 96,
+// 2 x 20 KB for d = 80), for d <= 64 in the slot or in a dS^T buffer.
 template <int D>
 struct DqChunks {
     static constexpr int N32 = D / 32;

@@ -44,18 +44,21 @@ struct Chunks {
 };
 
 // The head dimension in W-column chunks (W = 16: 32-byte rows and swizzle;
-// W = 32: 64-byte), unpadded: a d = 80 tile of 128 rows takes 20 KB with
-// W = 16 instead of the padded 32 KB.  The chunks are uniform, so a product
-// whose N is the head dim is still one instruction (N-direction atoms of W
-// columns, one chunk apart), and a k-step over d stays inside one chunk.
+// W = 32: 64-byte), the last one padded to W columns when W does not divide
+// d (the TMA fills the columns past d with zeros).  A d = 80 tile of 128 rows
+// takes 20 KB with W = 16 and 24 KB with W = 32 instead of 32 KB in 64-column
+// chunks.  The chunks are uniform, so a product whose N is the head dim is
+// still one instruction (N-direction atoms of W columns, one chunk apart); the
+// k-steps over d stop at d.
 template <int D, int W>
 struct ChunksW {
-    static_assert((W == 16 || W == 32) && D % W == 0, "uniform 16- or 32-column chunks");
-    static constexpr int NCH = D / W;
-    __host__ __device__ static constexpr int width(int) { return W; }
+    static_assert((W == 16 || W == 32) && D % 16 == 0, "16- or 32-column chunks, d a multiple of 16");
+    static constexpr int NCH = (D + W - 1) / W;
+    static constexpr int COLS = NCH * W;                      // head-dim columns stored per row
+    __host__ __device__ static constexpr int width(int c) { return c < NCH - 1 ? W : D - W * (NCH - 1); }
     __host__ __device__ static constexpr int col(int c) { return W * c; }
     __host__ __device__ static constexpr int tile_off(int c, int rows) { return c * rows * W * 2; }
-    __host__ __device__ static constexpr int tile_bytes(int rows) { return rows * D * 2; }
+    __host__ __device__ static constexpr int tile_bytes(int rows) { return rows * COLS * 2; }
     __host__ __device__ static constexpr uint32_t swz(int) { return W == 16 ? SW_32B : SW_64B; }
     __host__ __device__ static constexpr int row_bytes(int) { return W * 2; }
     __host__ __device__ static constexpr int map_index(int) { return 1; }
