@@ -13,8 +13,9 @@
 //   dQ_i = dS K                    (Eq. 18; the same shared-memory dS^T tile
 //                                   read as an M-major operand)
 // dQ_i leaves Tensor Memory through a separate warpgroup: it stages the fp32
-// tile in shared memory (in the slot of Q_i / dO_i, which the products no
-// longer need) and adds it into the fp32 dQ accumulator with TMA bulk
+// tile in shared memory (for d > 64 in the slot of Q_i / dO_i, which the
+// products no longer need; for d = 64 in a buffer of its own, 32 columns at a
+// time) and adds it into the fp32 dQ accumulator with TMA bulk
 // reduce-adds, whole 128-byte lines at a time (the stated dQ strategy: atomic
 // accumulation across key tiles).  The scale of Eq. 18 is applied when the
 // accumulator is converted, that of Eq. 19 when dK is written.
@@ -75,6 +76,11 @@ struct BwdTm {
     // d <= 32: dQ_i is issued by a second thread (in the dQ read-out warps);
     // its products are the cheapest, so one issuing thread limits the most.
     static constexpr bool SPLIT_DQ = D <= 32;
+    // d = 64: dQ_i is staged for the reduce-add in a 16 KB buffer of its own,
+    // one 32-column chunk at a time, so that the Q_i / dO_i slot is free as
+    // soon as dK has read it (the reduce-add reads ~20 bytes per clock: a
+    // slot held until then kept the next loads, and so the next S^T, waiting).
+    static constexpr bool DQSTAGE = PIPE && !SPLIT_DQ;
     static constexpr uint32_t DV = 0;
     static constexpr uint32_t DK = PIPE ? 64 : 128;
     static constexpr uint32_t DQ = PIPE ? 128 : TM_DP;
@@ -101,7 +107,8 @@ struct BwdCfg {
     static constexpr int DS_BYTES = BK * BQ * 2;
     static constexpr int NDS = BwdTm<D>::PIPE ? 2 : 1;      // dS^T buffers
     static constexpr int LD_BYTES = BQ * 8;            // (L * log2 e, D) per query row
-    static constexpr int FIXED = 2 * TILE + NDS * DS_BYTES;  // K, V, dS^T
+    static constexpr int DQS_BYTES = BwdTm<D>::DQSTAGE ? BQ * 32 * 4 : 0;   // one fp32 dQ_i chunk
+    static constexpr int FIXED = 2 * TILE + NDS * DS_BYTES + DQS_BYTES;  // K, V, dS^T, dQ_i staging
     static constexpr int STAGE = 2 * TILE + LD_BYTES;  // [Q_i | dO_i], (L, D)_i
     static constexpr int NS_RAW = (SMEM_BUDGET - FIXED - 256) / STAGE;
     static constexpr int NS = NS_RAW > 3 ? 3 : NS_RAW;
@@ -110,10 +117,11 @@ struct BwdCfg {
     static constexpr int DS_OFF = 2 * TILE;
     static constexpr int QD_OFF = DS_OFF + NDS * DS_BYTES;   // stage s: Q at QD_OFF + 2*TILE*s, dO right after
     static constexpr int LD_OFF = QD_OFF + NS * 2 * TILE;
-    static constexpr int BAR_OFF = LD_OFF + NS * LD_BYTES;
+    static constexpr int DQS_OFF = LD_OFF + NS * LD_BYTES;   // 1024-byte aligned (128-byte swizzle)
+    static constexpr int BAR_OFF = DQS_OFF + DQS_BYTES;
     // kv_full, q_full[NS], q_empty[NS], s_full, p_full, dq_full, dq_empty, stg, done, drain,
-    // s_free, p_free, ds_free[2], drain_dq, dp_full, dst_full
-    static constexpr int NBARS = 15 + 2 * NS;
+    // s_free, p_free, ds_free[2], drain_dq, dp_full, dst_full, stg_free
+    static constexpr int NBARS = 16 + 2 * NS;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int DYN_SMEM = (BYTES + 1024) <= SMEM_BUDGET ? (BYTES + 1024) : BYTES;
@@ -209,6 +217,7 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
     const uint32_t drain_dq = s_full + 88;    // the dQ issuer's products have finished (abort only)
     const uint32_t dp_full = s_full + 96;     // d > 64: dP^T is in Tensor Memory (s_full: S^T alone)
     const uint32_t dst_full = s_full + 104;   // d > 64: dS^T is in shared memory (p_full: P^T alone)
+    const uint32_t stg_free = s_full + 112;   // d = 64: the reduce-add has read the dQ_i staging buffer
     using TM = BwdTm<D>;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::MISC_OFF);
     volatile int* abort = reinterpret_cast<volatile int*>(smem + G::MISC_OFF + 4);
@@ -239,11 +248,10 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
         for (int s = 0; s < NS; ++s) {
             mbar_init(q_full(s), 33);        // TMA expect-tx arrival + 32 lanes that stage (L, D)
             // The slot is free once its last readers are done: dV and dK (the
-            // MMA issuer's commit) and, where dQ_i is staged in it, the dQ
-            // reduce-add's read (d = 64: both; d > 64: the reduce alone, whose
-            // dQ_i follows dK on the same issuer; d <= 32 and the dK/dV-only
-            // backward: the issuer alone).
-            mbar_init(q_empty(s), (WITH_DQ && TM::PIPE && !TM::SPLIT_DQ) ? 2 : 1);
+            // MMA issuer's commit; d <= 64 and the dK/dV-only backward) or, for
+            // d > 64, where dQ_i is staged in it, the dQ reduce-add's read
+            // (dQ_i follows dK on the same issuer).
+            mbar_init(q_empty(s), 1);
         }
         mbar_init(s_full, 1);
         mbar_init(p_full, 2 * BK);
@@ -259,6 +267,7 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
         mbar_init(drain_dq, 1);
         mbar_init(dp_full, 1);
         mbar_init(dst_full, 2 * BK);
+        mbar_init(stg_free, 1);
         *abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -714,15 +723,60 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 __syncwarp();
             }
             if (!warp_wait(dq_full, it & 1, abort, p.status)) break;
+            if constexpr (TM::DQSTAGE) {
+                // All of dQ_i into registers (its columns are then free for
+                // dQ_{i+1}), then chunk by chunk through the staging buffer.
+                tc_fence_after();
+                uint32_t r[QC::NCH][32];
+#pragma unroll
+                for (int cq = 0; cq < QC::NCH; ++cq) tmem_ld32(tQ + 32 * cq, r[cq]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int cq = 0; cq < QC::NCH; ++cq) reg_fence<32>(r[cq]);
+                tc_fence_before();
+                mbar_arrive(dq_empty);
+                const uint32_t buf = sb + G::DQS_OFF;
+                const int q0 = (i0 + it) * BQ;
+                bool st_ok = true;
+#pragma unroll
+                for (int cq = 0; cq < QC::NCH; ++cq) {
+                    static_assert(QC::NCH * 32 == D, "32-column dQ chunks");
+                    const int k = it * QC::NCH + cq;             // staging round
+                    if (k > 0 && !(st_ok = warp_wait(stg_free, (k - 1) & 1, abort, p.status))) break;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t off = (uint32_t)qr * 128 + (uint32_t)u * 16;
+                        const uint32_t phys = off ^ (((off >> 7) & 7u) << 4);
+                        st_shared_v4(buf + phys, r[cq][4 * u], r[cq][4 * u + 1], r[cq][4 * u + 2], r[cq][4 * u + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(stg);
+                    int lead_ok = 1;
+                    if (leader) {
+                        if (mbar_wait(stg, k & 1, abort, p.status, WAIT_LIMIT_NS)) {
+                            tma_reduce_add_3d(&p.tdq[QC::map_index(cq)], buf, cq * 32, q0, bh);
+                            bulk_commit();
+                            bulk_wait_read();
+                            mbar_arrive(stg_free);             // the buffer may take the next chunk
+                        } else {
+                            lead_ok = 0;
+                        }
+                    }
+                    if ((warp == DQ_WARP0) && __shfl_sync(0xffffffffu, lead_ok, 0) == 0) {
+                        st_ok = false;
+                        break;
+                    }
+                }
+                if (!st_ok) break;
+                continue;
+            }
             // d <= 32: dK (the other issuer's) must also have read dS^T before
             // the tile is staged over it; its commit completes q_empty.
             if (TM::SPLIT_DQ && !warp_wait(q_empty(s), (it / NS) & 1, abort, p.status)) break;
             tc_fence_after();
             // Stage this row box by box in the TMA swizzle: for d <= 32 into
-            // the dS^T buffer that dK and dQ_i have just read, otherwise into
-            // the Q_i / dO_i slot, whose readers finished before dQ_i did (the
-            // dS^T buffer is then released by the issuer as soon as dQ_i has
-            // read it, instead of after the reduce-add's slow read).
+            // the dS^T buffer that dK and dQ_i have just read, for d > 64 into
+            // the Q_i / dO_i slot, whose readers finished before dQ_i did.
             constexpr bool IN_DS = TM::PIPE && TM::SPLIT_DQ;
             const uint32_t slot = IN_DS ? sb + G::DS_OFF + (uint32_t)((it & 1) * G::DS_BYTES) : q_slot(s);
 #pragma unroll
