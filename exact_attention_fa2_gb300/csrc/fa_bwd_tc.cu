@@ -534,27 +534,29 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                 }
             };
             if constexpr (TM::PIPE) {
+                // Four 16-query groups; the Tensor Memory loads of group g+1
+                // are in flight while group g is computed.
+                uint32_t bs[2][16], bp[2][16];
+                uint32_t pk[16], dsp[16];
+                tmem_ld16(tS + 64 * h, bs[0]);
+                tmem_ld16(tP + 64 * h, bp[0]);
+                tmem_wait_ld();
+                reg_fence<16>(bs[0]);
+                reg_fence<16>(bp[0]);
 #pragma unroll
-                for (int qh = 0; qh < 2; ++qh) {
-                    const int qq = 2 * h + qh;                                  // 32-query quarter of the tile
-                    uint32_t rs[32], rp[32];
-                    tmem_ld32(tS + 32 * qq, rs);
-                    tmem_ld32(tP + 32 * qq, rp);
-                    tmem_wait_ld();
-                    reg_fence<32>(rs);
-                    reg_fence<32>(rp);
-                    if (qh == 1) {
-                        tc_fence_before();
-                        mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
+                for (int g = 0; g < 4; ++g) {
+                    const int cur = g & 1;
+                    if (g < 3) {
+                        tmem_ld16(tS + 64 * h + 16 * (g + 1), bs[cur ^ 1]);
+                        tmem_ld16(tP + 64 * h + 16 * (g + 1), bp[cur ^ 1]);
                     }
-                    uint32_t pk[16], dsp[16];
                     // P = exp2(S c - L2) and dS = P (dP - D) in f32x2 pairs; only
                     // the diagonal tile and a ragged key tile need the mask.
                     auto pair = [&](int e, bool mask) {
-                        const int q = 32 * qq + 2 * e;                          // query column inside the tile
+                        const int q = 64 * h + 16 * g + 2 * e;                   // query column inside the tile
                         const float4 ld = ld_shared_f4(ldb + q * 8);           // (-L2, -D) of q and q+1
                         float p0, p1;
-                        f2unpack(fma2(f2pack(__uint_as_float(rs[2 * e]), __uint_as_float(rs[2 * e + 1])), c2,
+                        f2unpack(fma2(f2pack(__uint_as_float(bs[cur][2 * e]), __uint_as_float(bs[cur][2 * e + 1])), c2,
                                       f2pack(ld.x, ld.y)), p0, p1);
                         p0 = ex2(p0);
                         p1 = ex2(p1);
@@ -564,27 +566,39 @@ __global__ void __launch_bounds__(bwd_threads<D>(), 1) bwd_tc_kernel(const __gri
                         }
                         const uint64_t p2 = f2pack(p0, p1);
                         float d0, d1;
-                        f2unpack(mul2(p2, add2(f2pack(__uint_as_float(rp[2 * e]), __uint_as_float(rp[2 * e + 1])),
+                        f2unpack(mul2(p2, add2(f2pack(__uint_as_float(bp[cur][2 * e]), __uint_as_float(bp[cur][2 * e + 1])),
                                                f2pack(ld.z, ld.w))), d0, d1);
-                        pk[e] = pack_bf16(p0, p1);
-                        dsp[e] = pack_bf16(d0, d1);
+                        pk[8 * cur + e] = pack_bf16(p0, p1);
+                        dsp[8 * cur + e] = pack_bf16(d0, d1);
                     };
                     if (diag || !key_ok) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) pair(e, true);
+                        for (int e = 0; e < 8; ++e) pair(e, true);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) pair(e, false);
+                        for (int e = 0; e < 8; ++e) pair(e, false);
                     }
-                    if (qh == 0) {
-                        // P^T and dS^T buffers of earlier tiles must have been read.
-                        if (it > 0 && !(ok = warp_wait(p_free, (it - 1) & 1, abort, p.status))) break;
-                        if (it > 1 && !(ok = warp_wait(ds_free(it & 1), ((it >> 1) - 1) & 1, abort, p.status))) break;
-                        tc_fence_after();
+                    if (g < 3) {
+                        tmem_wait_ld();
+                        reg_fence<16>(bs[cur ^ 1]);
+                        reg_fence<16>(bp[cur ^ 1]);
                     }
-                    // P^T of these 32 queries: 16 columns of bf16 pairs.
-                    tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
-                    store_ds(qh, dsp);
+                    if (g == 2) {
+                        tc_fence_before();
+                        mbar_arrive(s_free);                       // S^T / dP^T columns may take the next tile
+                    }
+                    if (cur == 1) {
+                        const int qh = g >> 1;
+                        if (qh == 0) {
+                            // P^T and dS^T buffers of earlier tiles must have been read.
+                            if (it > 0 && !(ok = warp_wait(p_free, (it - 1) & 1, abort, p.status))) break;
+                            if (it > 1 && !(ok = warp_wait(ds_free(it & 1), ((it >> 1) - 1) & 1, abort, p.status))) break;
+                            tc_fence_after();
+                        }
+                        // P^T of these 32 queries: 16 columns of bf16 pairs.
+                        tmem_st16(tmem + lane_off + TM::p_col(h, qh), pk);
+                        store_ds(qh, dsp);
+                    }
                 }
             } else {
                 // d > 64, in two phases: P^T from S^T (the exponentials) as soon
