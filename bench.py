@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--lean", action="store_true",
                     help="only the fwd+bwd steps of --workload (warm-up and timed), one short JSON line: "
                          "the command the ncu captures run, with nothing else on the device")
+    ap.add_argument("--non-causal", action="store_true",
+                    help="with --lean: the workload without the causal mask")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="with --lean: the step's backward through fa_bwd_deterministic")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--memory", action="store_true",
                     help="instead of timing: peak device memory of fwd+bwd against a materialised-score "
@@ -81,7 +85,7 @@ def flops_fwd(w: Workload, causal=True) -> float:
 def workload_config(w: Workload, causal: bool) -> dict:
     """The keys of the JSON line's `config` that name the workload; both arms
     report them alike and add their own timing keys."""
-    return {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} causal {w.dtype}",
+    return {"workload": f"{w.name}: B{w.B} H{w.H} S{w.S} d{w.d} {'causal' if causal else 'non-causal'} {w.dtype}",
             "B": w.B, "H": w.H, "S": w.S, "d": w.d, "causal": causal}
 
 
@@ -361,7 +365,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     fa.load_library()
     w = workload(args.workload)
-    causal = True
+    if (args.non_causal or args.deterministic) and not args.lean:
+        raise SystemExit("--non-causal and --deterministic are options of --lean")
+    causal = not args.non_causal
     scale = w.scale
     q, k, v, do = make_inputs(w.B, w.H, w.S, w.d, w.dtype, w.seed + 7919 * rank, w.qkv_scale)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
@@ -374,7 +380,8 @@ def run_ours(args, world, rank, local):
 
     def step():
         fa.fwd(qd, kd, vd, causal, scale, out=od, lse=lsed)
-        fa.bwd(qd, kd, vd, od, dod, lsed, causal, scale, workspace=ws, out=(dqd, dkd, dvd))
+        fa.bwd(qd, kd, vd, od, dod, lsed, causal, scale, workspace=ws, out=(dqd, dkd, dvd),
+               deterministic=args.deterministic)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -396,6 +403,7 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             f = 3.5 * flops_fwd(w, causal)
             print(json.dumps({"lean": True, "workload": workload_config(w, causal)["workload"],
+                              "deterministic_bwd": args.deterministic,
                               "ms_per_step": ms_per_step, "value": world * f / (ms_per_step * 1e-3) / 1e12,
                               "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup}), flush=True)
         sampler.stop()

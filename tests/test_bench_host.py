@@ -35,6 +35,13 @@ def test_flop_count_is_two_products_per_head(bench):
     assert bench.flops_fwd(w, causal=True) == madds
 
 
+def test_workload_config_names_the_mask(bench):
+    w = bench.workload("c3")
+    assert bench.workload_config(w, True)["workload"].endswith(" causal bf16")
+    assert bench.workload_config(w, False)["workload"].endswith(" non-causal bf16")
+    assert bench.workload_config(w, False)["causal"] is False
+
+
 def test_workload_names(bench):
     w = bench.workload("sweep:8192:128")
     assert (w.B, w.H, w.S, w.d, w.dtype) == (1, 16, 8192, 128, "bf16")
