@@ -82,14 +82,16 @@ __device__ __forceinline__ void grid_unit(int b, int BH, int n_units, int grp, i
 
 // Heads per group of that order for a kernel whose CTAs each stream
 // `bytes_per_head` of their head's data from L2.  All heads (the plain
-// longest-first order) while every head's data fits 160 MB; beyond that, as
+// longest-first order) while every head's data fits `limit_mib` (160 MiB for
+// the key-tile-outer backward, 128 MiB, about the L2, for the dQ pass: the
+// limits measured fastest for each); beyond that, as
 // few heads as give the GPU two waves of units, within 64 MB, so the CTAs in
 // flight re-read a few heads' tiles from L2 instead of DRAM.  Smaller groups
 // than needed would cost more in load balance (the heaviest units of later
 // groups start late) than they save.
-inline int head_group(int BH, int n_units, double bytes_per_head) {
+inline int head_group(int BH, int n_units, double bytes_per_head, double limit_mib = 160.0) {
     constexpr double kMB = 1024.0 * 1024.0;
-    if (BH * bytes_per_head <= 160.0 * kMB) return BH;
+    if (BH * bytes_per_head <= limit_mib * kMB) return BH;
     int sms = 152, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int g = (2 * sms + n_units - 1) / n_units;
