@@ -902,7 +902,7 @@ cudaError_t bwd_tc_launch(const BwdArgs& a) {
     // their zero gradients are written by a separate launch.
     if (a.causal) p.n_kv = std::min(p.n_kv, p.n_q);
     // Each CTA streams its head's Q, dO (bf16) and, with dQ, the fp32 dQ rows.
-    p.grp = head_group(BH, p.n_kv, (4.0 + (WITH_DQ ? 4.0 : 0.0)) * a.S * D);
+    p.grp = head_group(BH, p.n_kv, (4.0 + (WITH_DQ ? 4.0 : 0.0)) * a.S * D, WITH_DQ ? 160.0 : 128.0);
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;

@@ -101,6 +101,7 @@ struct FwdParams {
     int H;
     int S;            // query rows
     int n_units;      // 256-row query blocks per head
+    int grp;          // heads per group of the grid order
     int Sk;           // key rows seen by the K/V tensor maps
     int n_kv;         // 128-key tiles in [0, Sk)
     int dshift;       // causal: key tile j is on query tile t's diagonal when j = t + dshift (<= 0)
@@ -156,10 +157,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) fwd_tc_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // One flat grid ordered rank-major: every head's longest causal block is
-    // dispatched before any head's next one (longest job first).
+    // dispatched before any head's next one (longest job first), within head
+    // groups when the heads' K and V would not stay in L2 together.
     const int BH = (int)(gridDim.x / (unsigned)p.n_units);
-    const int rank = (int)blockIdx.x / BH;
-    const int bh = (int)blockIdx.x - rank * BH;
+    int rank, bh;
+    if (p.grp >= BH) {
+        rank = (int)blockIdx.x / BH;
+        bh = (int)blockIdx.x - rank * BH;
+    } else {
+        grid_unit((int)blockIdx.x, BH, p.n_units, p.grp, rank, bh);
+    }
     const int bb = bh / p.H, hh = bh - bb * p.H;
     const int unit = p.causal ? (p.n_units - 1 - rank) : rank;
     const int S = p.S;
@@ -557,6 +564,10 @@ cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o
     p.H = a.H;
     p.S = a.S;
     p.n_units = (a.S + 2 * BM - 1) / (2 * BM);
+    // Each CTA streams its head's K and V (bf16): grouped from 128 MiB of K
+    // and V, so that a group's CTAs re-read them from L2 (B4 H32 S4096 d80:
+    // DRAM reads 1.11 GB -> 0.25 GB per launch, time -1 %).
+    p.grp = head_group(BH, p.n_units, 4.0 * Sk * D, 128.0);
     p.Sk = Sk;
     p.n_kv = (Sk + BN - 1) / BN;
     p.dshift = -(key_begin / BN);

@@ -83,8 +83,9 @@ __device__ __forceinline__ void grid_unit(int b, int BH, int n_units, int grp, i
 // Heads per group of that order for a kernel whose CTAs each stream
 // `bytes_per_head` of their head's data from L2.  All heads (the plain
 // longest-first order) while every head's data fits `limit_mib` (160 MiB for
-// the key-tile-outer backward, 128 MiB, about the L2, for the dQ pass: the
-// limits measured fastest for each); beyond that, as
+// the key-tile-outer backward with dQ, 128 MiB, about the L2, for the
+// forward, the dK/dV-only backward and the dQ pass: the limits measured
+// fastest for each); beyond that, as
 // few heads as give the GPU two waves of units, within 64 MB, so the CTAs in
 // flight re-read a few heads' tiles from L2 instead of DRAM.  Smaller groups
 // than needed would cost more in load balance (the heaviest units of later
