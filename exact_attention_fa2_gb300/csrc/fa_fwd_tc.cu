@@ -567,9 +567,8 @@ cudaError_t fwd_tc_launch(const FwdArgs& a, int key_begin, int key_end, float* o
     // Each CTA streams its head's K and V (bf16): grouped from 128 MiB of K
     // and V, so that a group's CTAs re-read them from L2 (B4 H32 S4096 d80:
     // DRAM reads 1.11 GB -> 0.25 GB per launch, time -1 %), and only with
-    // eight or more waves of units (B1 H16 S32768 d128, four, was 6 %
-    // slower grouped).
-    p.grp = head_group(BH, p.n_units, 4.0 * Sk * D, 128.0, 8);
+    // many heads (B1 H16 S32768 d128 was 7 % slower grouped).
+    p.grp = head_group(BH, p.n_units, 4.0 * Sk * D, 128.0, true);
     p.Sk = Sk;
     p.n_kv = (Sk + BN - 1) / BN;
     p.dshift = -(key_begin / BN);

@@ -90,14 +90,17 @@ __device__ __forceinline__ void grid_unit(int b, int BH, int n_units, int grp, i
 // flight re-read a few heads' tiles from L2 instead of DRAM.  Smaller groups
 // than needed would cost more in load balance (the heaviest units of later
 // groups start late) than they save.
-inline int head_group(int BH, int n_units, double bytes_per_head, double limit_mib = 160.0, int min_waves = 0) {
+inline int head_group(int BH, int n_units, double bytes_per_head, double limit_mib = 160.0,
+                      bool only_many_heads = false) {
     constexpr double kMB = 1024.0 * 1024.0;
     if (BH * bytes_per_head <= limit_mib * kMB) return BH;
     int sms = 152, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // A later group's heaviest units start late; with fewer than `min_waves`
-    // waves of units such a unit is a large share of an SM's work.
-    if ((long long)BH * n_units < (long long)min_waves * sms) return BH;
+    // With fewer heads than a quarter of the SMs, the plain order already
+    // keeps four or more units of every head in flight, which re-read that
+    // head's tiles from L2, and grouping only delays later groups' heaviest
+    // units.
+    if (only_many_heads && 4 * BH < sms) return BH;
     int g = (2 * sms + n_units - 1) / n_units;
     const int cap = (int)(64.0 * kMB / bytes_per_head);
     g = g < cap ? g : cap;
