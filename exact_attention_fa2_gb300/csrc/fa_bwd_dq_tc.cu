@@ -412,8 +412,9 @@ cudaError_t bwd_dq_tc_launch(const BwdArgs& a) {
     p.n_kv = (a.Sk + BK - 1) / BK;
     // Each CTA streams its head's K and V (bf16).  Grouped from 128 MiB: at
     // B4 H32 S4096 d80 (160 MiB of K and V) grouping took this pass from 663
-    // to 622 us.
-    p.grp = head_group(a.B * a.H, p.n_q, 4.0 * a.Sk * D, 128.0);
+    // to 622 us.  As for the forward, which walks K and V the same way, only
+    // with many heads.
+    p.grp = head_group(a.B * a.H, p.n_q, 4.0 * a.Sk * D, 128.0, true);
     p.causal = a.causal;
     const float c = fabsf(a.scale) * FA_LOG2E;
     p.c = c < 1e-30f ? 1e-30f : c;
