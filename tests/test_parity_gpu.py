@@ -546,6 +546,27 @@ def test_deterministic_backward_c2_sampled_heads():
             assert_close(f"{name} deterministic [b={b},h={h}]", g[b, h], r[name], *TOL["bf16"]["grad"])
 
 
+def test_deterministic_backward_c4_every_head_group():
+    """The deterministic backward at c4 (B4 H32 S4096 d80, x2 inputs), where
+    its dQ pass orders the grid in groups of heads: repeat-exact, dK and dV
+    bit-identical to the atomic backward, and dQ on sampled rows of 15 heads
+    spread so that every run of 10 consecutive heads holds one (the last,
+    shorter group included) against the oracle."""
+    w = WORKLOADS["c4"]
+    q, k, v, do = make_workload_inputs(w)
+    atomic, det1, det2 = _bwd_both(q, k, v, do, True, w.scale)
+    for a, b in zip(det1, det2):
+        assert torch.equal(a, b)
+    assert torch.equal(det1[1], atomic[1]) and torch.equal(det1[2], atomic[2])
+    assert torch.isfinite(det1[0]).all()
+    for bh in list(range(0, w.B * w.H, 9)) + [w.B * w.H - 1]:
+        b, h = divmod(bh, w.H)
+        rows = sample_positions(w.S, 9600 + bh)
+        keys = sample_positions(w.S, 9800 + bh)[:4]
+        r = oracle_sampled_grads(q, k, v, do, b, h, rows, keys, True, w.scale, "bf16")
+        assert_close(f"dQ rows deterministic [b={b},h={h}]", det1[0][b, h, rows], r["dq"], *TOL["bf16"]["grad"])
+
+
 def test_deterministic_autograd_matches_atomic():
     q, k, v, do = make_inputs(1, 2, 384, 64, "bf16", seed=8200)
     grads = []
